@@ -1,0 +1,36 @@
+"""Float64 CPU oracle for exact tiled attention, flash-decoding and RMSNorm.
+
+TEST INFRASTRUCTURE ONLY. This package is the slow, obviously correct
+definition that the CUDA path is checked against. Only the tests, the smoke
+check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may
+import it; the library (``exact_tiled_attention_attn_gb300``) never does, and
+this package imports nothing from the library.
+
+Every function works in float64 on inputs decoded exactly from bfloat16, and
+cites the passage of the source pages it writes out. The pages are:
+
+* "Module 07: Fused operators and FlashAttention" (LLM Inference Systems course)
+* "FlashAttention: attention without the n x n matrix" (GPU-internals lesson)
+* "Attention from the kernel's side: FlashAttention, online softmax and fused
+  dequantisation" (note, in Polish)
+* "Chapter 5. Operators and runtime", section 5.3.3 "FlashAttention: tiling
+  and online softmax" (book chapter)
+
+Parity status: every function here is pinned by the tests in
+``tests/test_oracle_pins.py`` (worked examples printed on the pages, closed
+forms, brute force on tiny inputs, and the recurrence-equals-three-pass
+identity). No function is "parity unpinned".
+"""
+from .attention import (  # noqa: F401
+    scores_softmax_weighted,
+    online_softmax_blocks,
+    online_normalizer,
+    online_weighted_stream,
+    attention,
+    attention_rows,
+    attention_online,
+    decode,
+    decode_split_merge,
+    count_blocks,
+)
+from .rmsnorm import rmsnorm, rmsnorm_rows  # noqa: F401
