@@ -1,0 +1,145 @@
+"""Exact tiled attention, flash-decoding and fused RMSNorm for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libgb300attn.so`` (``include/attn.h``).
+The binding only checks and marshals arguments (torch tensors -> device
+pointers, the current CUDA stream); every step of the computation runs in the
+library's CUDA kernels. PyTorch provides device memory and streams.
+
+    o, lse = fwd(q, k, v, causal=True)             # q [B,Hq,T,d], k/v [B,Hkv,T,d], bf16
+    o, lse = decode(q, kcache, vcache, seqlens)     # q [B,Hq,d], caches [B,Hkv,Lcap,d]
+    y = rmsnorm(x, w, eps=1e-6)                     # x [T,D], w [D]
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+from ._lib import AttnError  # noqa: F401
+
+__all__ = ["fwd", "decode", "rmsnorm", "decode_workspace_size", "default_splits",
+           "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _lib.load()
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_tensor(name, t, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+        return_lse: bool = True, stream=None):
+    """Exact attention O = softmax(scale * Q K^T + mask) V (bf16 in/out), and the fp32 LSE.
+
+    q [B, Hq, Tq, d], k/v [B, Hkv, Tk, d], contiguous bf16 on one CUDA device.
+    """
+    _check_tensor("q", q, torch.bfloat16, 4)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must both be [B, Hkv, Tk, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor("out", out, torch.bfloat16, 4)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else None,
+                              B, Hq, Hkv, Tq, Tk, d, 1 if causal else 0, float(scale), _stream_ptr(stream))
+    _lib.check("attn_fwd", st)
+    return out, lse
+
+
+def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
+    return int(_lib.load().attn_decode_workspace_size(B, Hq, d, num_splits))
+
+
+def default_splits(B: int, Hkv: int, Lcap: int) -> int:
+    return int(_lib.load().attn_decode_default_splits(B, Hkv, Lcap))
+
+
+def decode(q, kcache, vcache, seqlens, scale: float | None = None, num_splits: int | None = None,
+           workspace=None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Flash-decoding: one query per sequence against a bf16 KV cache.
+
+    q [B, Hq, d]; kcache/vcache [B, Hkv, Lcap, d]; seqlens int32 [B] on the device.
+    ``workspace`` (uint8 tensor) is allocated when not given.
+    """
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("kcache", kcache, torch.bfloat16, 4)
+    _check_tensor("vcache", vcache, torch.bfloat16, 4)
+    _check_tensor("seqlens", seqlens, torch.int32, 1)
+    B, Hq, d = q.shape
+    Hkv, Lcap = kcache.shape[1], kcache.shape[2]
+    if kcache.shape != vcache.shape or kcache.shape[0] != B or kcache.shape[3] != d:
+        raise ValueError("kcache and vcache must both be [B, Hkv, Lcap, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        num_splits = default_splits(B, Hkv, Lcap)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_decode(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), seqlens.data_ptr(),
+                                 out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                 B, Hq, Hkv, d, Lcap, float(scale), int(num_splits),
+                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream))
+    _lib.check("attn_decode", st)
+    return out, lse
+
+
+def rmsnorm(x, w, eps: float = 1e-6, out=None, stream=None):
+    """Fused RMSNorm y = x / sqrt(mean(x^2) + eps) * w over the last axis; bf16 in/out."""
+    _check_tensor("x", x, torch.bfloat16, 2)
+    _check_tensor("w", w, torch.bfloat16, 1)
+    T, D = x.shape
+    if w.shape[0] != D:
+        raise ValueError("w must have D elements")
+    if out is None:
+        out = torch.empty_like(x)
+    st = _lib.load().rmsnorm_fwd(x.data_ptr(), w.data_ptr(), out.data_ptr(), T, D, float(eps),
+                                 _stream_ptr(stream))
+    _lib.check("rmsnorm_fwd", st)
+    return out
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status code."""
+    return int(_lib.load().attn_last_device_error(_stream_ptr(stream)))
+
+
+def kernel_launches() -> int:
+    return int(_lib.load().attn_kernel_launches())
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    _lib.check("attn_selftest_wait_timeout",
+               _lib.load().attn_selftest_wait_timeout(int(timeout_us), _stream_ptr(stream)))

@@ -1,0 +1,156 @@
+// api.cu - the library's C ABI (include/attn.h): argument validation, dispatch to the
+// kernels, device error reporting and the launch counter.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace gb300 {
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                            int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream);
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens, void* o, float* lse,
+                          int B, int Hq, int Hkv, int d, int Lcap, float scale, int S, int C, void* workspace,
+                          cudaStream_t stream, int* launched);
+cudaError_t launch_rmsnorm(const void* x, const void* w, void* y, int T, int D, float eps, cudaStream_t s);
+uint32_t prefill_take_device_error();
+uint32_t decode_take_device_error();
+uint32_t rmsnorm_take_device_error();
+
+static std::atomic<unsigned long long> g_launches{0};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int decode_chunk(int Lcap, int num_splits) {
+  const long long c = (static_cast<long long>(Lcap) + num_splits - 1) / num_splits;
+  return static_cast<int>((c + 15) / 16 * 16);
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait gives up.
+__global__ void selftest_wait_kernel(uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, timeout_ns);
+  __syncthreads();
+}
+
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return ATTN_ERR_INVALID_ARG;
+  const cudaError_t err = launch_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
+  if (err != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || d < 1 || num_splits < 1) return 0;
+  return static_cast<size_t>(B) * Hq * num_splits * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+int attn_decode_default_splits(int B, int Hkv, int Lcap) {
+  if (B < 1 || Hkv < 1 || Lcap < 1) return 1;
+  // Chunks of about 512 keys; at least enough splits for ~4 thread blocks per SM
+  // of a 152-SM part when the batch is small.
+  int s = (Lcap + 511) / 512;
+  const long long want = (4LL * 152 + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
+  if (s < want) s = static_cast<int>(want);
+  const int smax = (Lcap + 15) / 16;
+  if (s > smax) s = smax;
+  return s < 1 ? 1 : s;
+}
+
+attn_status attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
+                        float* lse, int B, int Hq, int Hkv, int d, int Lcap, float scale, int num_splits,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < attn_decode_workspace_size(B, Hq, d, num_splits))
+    return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  const int C = decode_chunk(Lcap, num_splits);
+  int launched = 0;
+  const cudaError_t err = launch_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits,
+                                        C, workspace, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status rmsnorm_fwd(const void* x, const void* w, void* y, int T, int D, float eps, cudaStream_t stream) {
+  if (x == nullptr || w == nullptr || y == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (T < 1 || D < 8 || D % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID_ARG;
+  if (D > 8192) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ATTN_ERR_MISALIGNED;
+  const cudaError_t err = launch_rmsnorm(x, w, y, T, D, eps, stream);
+  if (err != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "pointer not aligned";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+attn_status attn_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  const uint32_t e = prefill_take_device_error() | decode_take_device_error() | rmsnorm_take_device_error() |
+                     take_device_error_word();
+  if (e == 0xFFFFFFFFu) return ATTN_ERR_CUDA;
+  if (e & kErrTimeout) return ATTN_ERR_TIMEOUT;
+  return ATTN_OK;
+}
+
+unsigned long long attn_kernel_launches(void) { return g_launches.load(); }
+
+attn_status attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return ATTN_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(timeout_us) * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+}  // extern "C"

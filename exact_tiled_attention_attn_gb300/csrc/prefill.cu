@@ -1,0 +1,454 @@
+// prefill.cu - exact tiled attention forward pass on 5th-generation tensor cores (sm_103a).
+//
+// What it computes ("FlashAttention: attention without the n x n matrix", section
+// "Forward pass of FlashAttention"; "Module 07: Fused operators and FlashAttention",
+// sections "Online softmax: derivation" and "FlashAttention-2"): for a block of
+// 128 query rows, walk the key/value blocks of 128 keys, keep per row the running
+// maximum m, the running sum l and the unnormalised output O, rescale l and O by
+// 2^(m_old - m_new) when the maximum moves, and divide once at the end. Key blocks
+// entirely above the diagonal are never visited when causal; the element mask is
+// applied only on blocks that cross the diagonal or the end of the keys.
+//
+// How it maps onto the GPU (one CTA per work unit of two 128-row query tiles that
+// share one K/V stream: two query heads of the same K/V group at the same rows, or,
+// when the group size is odd, two consecutive row tiles of one head):
+//   warp 8      TMA producer: Q tiles once, then K and V tiles into 2-3 stage rings
+//               (128-byte swizzled boxes of 64 columns x 128 rows).
+//   warp 9      MMA issuer (one thread): S_q = Q_q K^T into TMEM (fp32), then
+//               O_q += P_q V with P read from TMEM (bf16) and V from shared memory.
+//   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1: one thread owns one
+//               row (TMEM lane), so row max and row sum need no shuffles; P is
+//               written back into the TMEM columns of S; O is rescaled in TMEM.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
+// P_q aliases the first 64 columns of S_q.
+//
+// The maximum used as the exponent base is only moved when the new block maximum
+// exceeds it by more than 2^8 (in base 2); the normalised result does not depend on
+// which finite base is subtracted ("Module 07", section "Online softmax: derivation":
+// the factor exp(m - c) cancels between numerator and denominator), and the bound
+// keeps every p <= 256, far inside fp32 and bf16 range.
+#include "common.cuh"
+
+namespace gb300 {
+
+constexpr uint64_t kPrefillWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr float kRescaleThreshold = 8.0f;                   // log2 of the allowed growth of p
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int kBM = 128;                  // query rows per tile
+  static constexpr int kBN = 128;                  // keys per tile
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kBoxBytes = 128 * 128;      // 128 rows x 64 bf16 columns
+  static constexpr int kNumBox = D / 64;
+  static constexpr int kTileBytes = kNumBox * kBoxBytes;
+  static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+  static constexpr int kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kIdescQK = make_idesc_bf16_f32(128, 128, false);
+  static constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, D, true);
+};
+
+struct PrefillParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int B, Hq, Hkv, Tq, Tk, g;
+  int causal;
+  int pair_heads;  // 1: tiles are heads (2p, 2p+1) at the same rows; 0: row tiles (2p, 2p+1) of one head
+  int n_qt;        // number of query tiles of 128 rows
+  float c;         // scale * log2(e)
+};
+
+struct UnitInfo {
+  int b, kvh;
+  int head[2];
+  int row0[2];
+  int nkv[2];  // key tiles to visit per query tile (0 = tile inactive)
+};
+
+__device__ __forceinline__ int kv_tiles_for(const PrefillParams& p, int row0) {
+  if (row0 >= p.Tq) return 0;
+  const int all = (p.Tk + 127) / 128;
+  if (!p.causal) return all;
+  const int last_row = min(row0 + 127, p.Tq - 1);
+  return min(all, last_row / 128 + 1);
+}
+
+__device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit) {
+  UnitInfo u;
+  if (p.pair_heads) {
+    const int hp_count = p.Hq / 2;
+    const int per_rank = hp_count * p.B;
+    const int rank = unit / per_rank;
+    const int rest = unit % per_rank;
+    const int hp = rest % hp_count;
+    u.b = rest / hp_count;
+    const int qt = p.causal ? (p.n_qt - 1 - rank) : rank;  // heaviest tiles first when causal
+    u.head[0] = 2 * hp;
+    u.head[1] = 2 * hp + 1;
+    u.row0[0] = u.row0[1] = qt * 128;
+  } else {
+    const int n_pairs = (p.n_qt + 1) / 2;
+    const int per_rank = p.Hq * p.B;
+    const int rank = unit / per_rank;
+    const int rest = unit % per_rank;
+    const int h = rest % p.Hq;
+    u.b = rest / p.Hq;
+    const int tp = p.causal ? (n_pairs - 1 - rank) : rank;
+    u.head[0] = u.head[1] = h;
+    u.row0[0] = 2 * tp * 128;
+    u.row0[1] = (2 * tp + 1) * 128;
+  }
+  u.kvh = u.head[0] / p.g;
+  u.nkv[0] = kv_tiles_for(p, u.row0[0]);
+  u.nkv[1] = kv_tiles_for(p, u.row0[1]);
+  return u;
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using Cfg = PrefillCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                           // [2][tile]
+  uint8_t* sK = smem + 2 * Cfg::kTileBytes;                     // [stages][tile]
+  uint8_t* sV = sK + Cfg::kStages * Cfg::kTileBytes;            // [stages][tile]
+
+  __shared__ uint64_t q_full;
+  __shared__ uint64_t k_full[Cfg::kStages], k_empty[Cfg::kStages];
+  __shared__ uint64_t v_full[Cfg::kStages], v_empty[Cfg::kStages];
+  __shared__ uint64_t s_full[2], p_full[2], o_done[2];
+  __shared__ uint64_t mma_drain;
+  __shared__ uint32_t tmem_base_holder;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const UnitInfo u = decode_unit(p, blockIdx.x);
+  const int n_iter = max(u.nkv[0], u.nkv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], 128);
+      mbar_init(&o_done[q], 1);
+    }
+    mbar_init(&mma_drain, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_base_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_holder;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      const int nq = (u.nkv[0] > 0) + (u.nkv[1] > 0);
+      mbar_arrive_expect_tx(&q_full, nq * Cfg::kTileBytes);
+      for (int q = 0; q < 2; ++q) {
+        if (u.nkv[q] == 0) continue;
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sQ + q * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmQ, &q_full, kb * 64, u.row0[q],
+                      u.b * p.Hq + u.head[q]);
+      }
+      const int zkv = u.b * p.Hkv + u.kvh;
+      int issued = 0;
+      for (int j = 0; j < n_iter; ++j) {
+        const int s = j % Cfg::kStages;
+        const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
+        if (!mbar_wait(&k_empty[s], ph ^ 1u, abort_p, kPrefillWaitTimeoutNs)) break;
+        mbar_arrive_expect_tx(&k_full[s], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sK + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmK, &k_full[s], kb * 64, j * 128, zkv);
+        if (!mbar_wait(&v_empty[s], ph ^ 1u, abort_p, kPrefillWaitTimeoutNs)) {
+          issued = j + 1;  // K of tile j is in flight, V is not
+          break;
+        }
+        mbar_arrive_expect_tx(&v_full[s], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmV, &v_full[s], kb * 64, j * 128, zkv);
+        issued = j + 1;
+      }
+      if (*abort_p) {
+        // Let the copies still in flight land before the CTA exits.
+        mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
+        for (int j = max(0, issued - Cfg::kStages); j < issued; ++j) {
+          const int s = j % Cfg::kStages;
+          const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
+          mbar_wait(&k_full[s], ph, abort_p, kPrefillWaitTimeoutNs);
+          mbar_wait(&v_full[s], ph, abort_p, kPrefillWaitTimeoutNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      bool ok = mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
+      tc_fence_after();
+      bool any_mma = false;
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % Cfg::kStages;
+        const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
+        if (!(ok = mbar_wait(&k_full[s], ph, abort_p, kPrefillWaitTimeoutNs))) break;
+        tc_fence_after();
+        for (int q = 0; q < 2 && ok; ++q) {
+          if (j >= u.nkv[q]) continue;
+          if (j > 0) {  // PV of the previous block read P from these columns
+            if (!(ok = mbar_wait(&o_done[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
+              break;
+            tc_fence_after();
+          }
+          const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
+            const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
+            const uint64_t db = make_sdesc_sw128(sKa + s * Cfg::kTileBytes + off, 16, 1024);
+            umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          any_mma = true;
+          umma_commit(&s_full[q]);
+        }
+        if (!ok) break;
+        umma_commit(&k_empty[s]);
+        if (!(ok = mbar_wait(&v_full[s], ph, abort_p, kPrefillWaitTimeoutNs))) break;
+        tc_fence_after();
+        for (int q = 0; q < 2 && ok; ++q) {
+          if (j >= u.nkv[q]) continue;
+          if (!(ok = mbar_wait(&p_full[q], static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
+          tc_fence_after();
+          const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
+          const uint32_t a_p = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+#pragma unroll
+          for (int kk = 0; kk < 128 / 16; ++kk) {
+            const uint64_t db = make_sdesc_sw128(sVa + s * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
+            umma_ts(d_o, a_p + kk * 8, db, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&o_done[q]);
+        }
+        if (!ok) break;
+        umma_commit(&v_empty[s]);
+      }
+      if (any_mma) {  // every MMA has finished before TMEM is released
+        umma_commit(&mma_drain);
+        mbar_wait(&mma_drain, 0, abort_p, kPrefillWaitTimeoutNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ softmax warps ------------------------------
+    const int q = warp >> 2;
+    const int wq = warp & 3;
+    const int nkv = q ? u.nkv[1] : u.nkv[0];
+    const int row0 = q ? u.row0[1] : u.row0[0];
+    const int head = q ? u.head[1] : u.head[0];
+    const int row_in_tile = wq * 32 + lane;
+    const int row = row0 + row_in_tile;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+    const uint32_t t_o = tmem + lane_off + (q ? Cfg::kTmO1 : Cfg::kTmO0);
+    const float c = p.c;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nkv; ++j) {
+      if (!(ok = mbar_wait(&s_full[q], static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128(t_s, sr);
+      const int j0 = j * 128;
+      const bool need_mask = (j0 + 128 > p.Tk) || (p.causal && j0 + 127 > row0);
+      if (need_mask) {
+        const int lim = p.causal ? min(p.Tk - 1, row) : (p.Tk - 1);  // last visible key of this row
+#pragma unroll
+        for (int k = 0; k < 128; ++k)
+          if (j0 + k > lim) sr[k] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+      for (int k = 4; k < 128; k += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[k + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[k + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[k + 3]));
+      }
+      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_cand = fmaxf(m_run, m_blk);
+      const bool grow = m_cand > m_run + kRescaleThreshold;
+      float corr = 1.f;
+      if (grow) {
+        corr = ex2_approx(m_run - m_cand);  // 0 when m_run = -inf
+        m_run = m_cand;
+      }
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+
+      const float nb = -base;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc * 32 + 2 * k]), c, nb));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc * 32 + 2 * k + 1]), c, nb));
+          sum0 += p0;
+          sum1 += p1;
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + cc * 16, pk);
+      }
+      l_run = l_run * corr + (sum0 + sum1);
+      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+        // O holds the sum up to block j-1 relative to the old base: wait for that PV, rescale in TMEM
+        // (done after P is written so the registers of S are free).
+        if (!(ok = mbar_wait(&o_done[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(t_o + cc * 32, ov);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * corr);
+          tmem_st32(t_o + cc * 32, ov);
+        }
+      }
+
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[q]);
+    }
+
+    if (ok && nkv > 0) {
+      ok = mbar_wait(&o_done[q], static_cast<uint32_t>(nkv - 1) & 1u, abort_p, kPrefillWaitTimeoutNs);
+      tc_fence_after();
+      if (ok) {
+        const float inv_l = 1.f / l_run;
+        const bool store = row < p.Tq;
+        const size_t orow = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(t_o + cc * 32, ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv_l, __uint_as_float(ov[2 * k + 1]) * inv_l);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (store && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// --------------------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// --------------------------------------------------------------------------------------
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled get_encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// 3-D map over a [Z, rows, D] bf16 tensor, box = 64 columns x 128 rows x 1, 128-byte swizzle,
+// out-of-range rows read as zero.
+static bool make_map_3d(CUtensorMap* map, const void* base, int D, int rows, int Z) {
+  PFN_encodeTiled enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(Z)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                const PrefillParams& p, int units, cudaStream_t stream) {
+  using Cfg = PrefillCfg<D>;
+  auto kern = attn_fwd_kernel<D>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+// Returns cudaErrorInvalidValue if a tensor map cannot be built (e.g. driver entry point missing).
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map_3d(&mq, q, d, Tq, B * Hq) || !make_map_3d(&mk, k, d, Tk, B * Hkv) ||
+      !make_map_3d(&mv, v, d, Tk, B * Hkv))
+    return cudaErrorInvalidValue;
+  PrefillParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Tq = Tq;
+  p.Tk = Tk;
+  p.g = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.pair_heads = (p.g % 2 == 0) ? 1 : 0;
+  p.n_qt = (Tq + 127) / 128;
+  p.c = scale * 1.4426950408889634f;
+  const long long units =
+      p.pair_heads ? static_cast<long long>(p.n_qt) * (Hq / 2) * B : static_cast<long long>((p.n_qt + 1) / 2) * Hq * B;
+  if (units <= 0 || units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, static_cast<int>(units), stream)
+                 : launch_fwd_d<128>(mq, mk, mv, p, static_cast<int>(units), stream);
+}
+
+uint32_t prefill_take_device_error() { return take_device_error_word(); }
+
+}  // namespace gb300

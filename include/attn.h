@@ -1,0 +1,175 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) exact tiled attention library.
+ *
+ * Three operations, each a plain-pointer call that launches hand-written
+ * CUDA kernels on the caller's stream:
+ *
+ *   attn_fwd     exact attention O = softmax(scale * Q K^T + causal mask) V for
+ *                many queries (prefill), with grouped-query heads, computed
+ *                tile by tile with the online-softmax recurrence so the score
+ *                matrix never reaches global memory.
+ *   attn_decode  the same for one query per sequence over a KV cache
+ *                (flash-decoding: the key range is split across thread blocks,
+ *                each writes a partial (m, l, o), a second kernel merges them).
+ *   rmsnorm_fwd  fused one-pass RMSNorm, one row per warp.
+ *
+ * Conventions shared by every entry point
+ * - All tensor pointers are DEVICE pointers to memory the caller owns; the
+ *   library never allocates, frees or keeps them. "bf16" means IEEE bfloat16
+ *   bit patterns (2 bytes, e.g. __nv_bfloat16 / torch.bfloat16).
+ * - Layouts are dense row-major with the last dimension contiguous.
+ * - Every call is asynchronous on `stream` (NULL = legacy default stream).
+ *   The return value reports argument validation and launch errors only;
+ *   inputs are never modified. Errors detected on the device (a bounded wait
+ *   that timed out) are reported by attn_last_device_error().
+ * - On any non-OK return nothing has been launched, except ATTN_ERR_CUDA,
+ *   which may follow a failed launch.
+ */
+#ifndef GB300_ATTN_H_
+#define GB300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, bad ratio, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented here (e.g. head dim not 64/128) */
+  ATTN_ERR_MISALIGNED = 3,   /* pointer not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than attn_decode_workspace_size() */
+  ATTN_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  ATTN_ERR_TIMEOUT = 6       /* a device-side bounded wait expired (reported by attn_last_device_error) */
+} attn_status;
+
+/*
+ * attn_fwd - exact scaled-dot-product attention for a batch of sequences.
+ *
+ * Defined by: "FlashAttention: attention without the n x n matrix", section
+ * "Forward pass of FlashAttention" (block update of m, l and the accumulator,
+ * O = A / l once at the end, and L = m + log l kept per row); "Module 07:
+ * Fused operators and FlashAttention", sections "Online softmax: derivation"
+ * and "FlashAttention-2" (query-block outer loop, causal block skipping);
+ * grouped-query heads as in "Attention from the kernel's side", section
+ * "Prefill and decoding are different problems".
+ *
+ *   q    bf16 [B, Hq,  Tq, d]      queries
+ *   k    bf16 [B, Hkv, Tk, d]      keys;   query head h reads K/V head h / (Hq/Hkv)
+ *   v    bf16 [B, Hkv, Tk, d]      values
+ *   o    bf16 [B, Hq,  Tq, d]      output (written)
+ *   lse  fp32 [B, Hq,  Tq] or NULL natural-log log-sum-exp of the scaled scores
+ *                                  of each row: ln sum_j exp(scale * q_i . k_j)
+ *   d      64 or 128 (else ATTN_ERR_UNSUPPORTED); Hq % Hkv == 0
+ *   causal 0: every key is visible; 1: key j is visible to query i iff j <= i
+ *          (aligned at the top-left corner when Tq != Tk)
+ *   scale  > 0 and finite (1/sqrt(d) for standard attention)
+ * Arithmetic: bf16 inputs, fp32 scores and running statistics, P rounded to
+ * bf16 for the P.V product, fp32 accumulation, O rounded once to bf16.
+ * q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                     int causal, float scale, cudaStream_t stream);
+
+/*
+ * attn_decode_workspace_size - bytes of scratch attn_decode needs.
+ * Returns 0 for invalid arguments. The workspace holds one fp32 partial
+ * (m, l, o[d]) per (sequence, query head, split).
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * attn_decode_default_splits - a split count that fills the GPU for the given
+ * shape (enough thread blocks for every SM several times over). Any value in
+ * [1, Lcap/16] is valid; results differ between split counts by rounding only.
+ */
+int attn_decode_default_splits(int B, int Hkv, int Lcap);
+
+/*
+ * attn_decode - one query token per sequence against a bf16 KV cache
+ * (flash-decoding).
+ *
+ * Defined by: "Attention from the kernel's side: FlashAttention, online
+ * softmax and fused dequantisation", section "Prefill and decoding are
+ * different problems" (one query per sequence streams the whole cache; GQA
+ * loads each K/V tile once for g query heads; flash-decoding splits the key
+ * sequence across thread blocks, each computes a partial (m, l, o) and a
+ * last step merges them with the same rescaling rule). The merge rule is the
+ * step of "Module 07: Fused operators and FlashAttention", section "Online
+ * softmax: derivation".
+ *
+ *   q        bf16 [B, Hq, d]
+ *   kcache   bf16 [B, Hkv, Lcap, d]
+ *   vcache   bf16 [B, Hkv, Lcap, d]
+ *   seqlens  int32 [B] (device)  keys 0 .. seqlens[b]-1 of sequence b take part;
+ *            precondition 1 <= seqlens[b] <= Lcap. A value outside that range
+ *            is clamped on the device (0 or less gives O = 0, LSE = -inf).
+ *   o        bf16 [B, Hq, d]    output (written)
+ *   lse      fp32 [B, Hq] or NULL
+ *   d 64 or 128, Hq % Hkv == 0, Hq / Hkv <= 8, scale > 0 and finite
+ *   num_splits   1 .. ceil(Lcap / 16). Split s covers keys
+ *                [s*C, (s+1)*C) with C = ceil(Lcap / num_splits) rounded up
+ *                to a multiple of 16; splits are merged in a fixed order, so
+ *                the result is deterministic for a given num_splits.
+ *   workspace    device scratch of at least
+ *                attn_decode_workspace_size(B, Hq, d, num_splits) bytes, 16-byte
+ *                aligned, owned by the caller; it must not be used by another
+ *                call that can run at the same time.
+ */
+attn_status attn_decode(const void* q, const void* kcache, const void* vcache,
+                        const int* seqlens, void* o, float* lse,
+                        int B, int Hq, int Hkv, int d, int Lcap, float scale,
+                        int num_splits, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/*
+ * rmsnorm_fwd - y = x / sqrt(mean_j x_j^2 + eps) * w for every row, one pass.
+ *
+ * Defined by: "Module 07: Fused operators and FlashAttention", section
+ * "Fused RMSNorm" (the formula; sum of squares kept in registers, the row
+ * held by one warp, no x^2 tensor) and section "Assignment 07.1:
+ * fused_rms_norm" (eps under the root, mean over D).
+ *
+ *   x  bf16 [T, D], w bf16 [D], y bf16 [T, D] (written; may not alias x)
+ *   D  a multiple of 8, 8 <= D <= 8192; T >= 1; eps >= 0 and finite
+ * Arithmetic: fp32 sum of squares and scaling, y rounded once to bf16.
+ */
+attn_status rmsnorm_fwd(const void* x, const void* w, void* y, int T, int D, float eps,
+                        cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_status_string(attn_status s);
+
+/*
+ * attn_last_device_error - synchronise `stream`, then report and clear the
+ * library's device error word: ATTN_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last call, ATTN_ERR_CUDA if the stream reported a
+ * CUDA error, else ATTN_OK.
+ */
+attn_status attn_last_device_error(cudaStream_t stream);
+
+/*
+ * attn_kernel_launches - number of kernels this library has launched in this
+ * process (all devices, all streams). Used to count launches in a timed region.
+ */
+unsigned long long attn_kernel_launches(void);
+
+/*
+ * attn_selftest_wait_timeout - launch one block whose thread waits on a
+ * shared-memory barrier that nothing completes, with a bound of
+ * `timeout_us` microseconds (1 .. 1000000). The wait gives up, records
+ * ATTN_ERR_TIMEOUT in the device error word and the kernel returns; read it
+ * back with attn_last_device_error(). This exercises the same bounded-wait
+ * routine the attention kernels use, without hanging the GPU.
+ */
+attn_status attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H_ */

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects invalid arguments before launching anything.
+No call here reaches a kernel, so these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_tiled_attention_attn_gb300 import _lib
+from exact_tiled_attention_attn_gb300.build import ROOT, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)) - {"defined"}
+
+
+def test_header_and_binding_agree():
+    declared = _declared_functions()
+    assert declared == set(_lib.SIGNATURES), declared ^ set(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(0) == b"ok"
+
+
+def test_workspace_size_formula(lib):
+    assert lib.attn_decode_workspace_size(16, 32, 128, 64) == 16 * 32 * 64 * 130 * 4
+    assert lib.attn_decode_workspace_size(0, 32, 128, 64) == 0
+    assert lib.attn_decode_workspace_size(1, 1, 64, 0) == 0
+
+
+def test_default_splits_in_range(lib):
+    for B, Hkv, L in [(16, 8, 32768), (1, 1, 16), (1, 1, 100000), (64, 8, 2048)]:
+        s = lib.attn_decode_default_splits(B, Hkv, L)
+        assert 1 <= s <= (L + 15) // 16
+
+
+FAKE = 0x10000  # a non-null, 16-byte-aligned value that is never dereferenced
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=2, Hkv=1, Tq=8, Tk=8, d=64,
+             causal=0, scale=0.125, stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Tq"],
+                        a["Tk"], a["d"], a["causal"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(B=0), 1), (dict(Tq=0), 1), (dict(Tk=-1), 1),
+    (dict(Hq=3, Hkv=2), 1), (dict(scale=0.0), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1), (dict(causal=2), 1), (dict(d=96), 2), (dict(d=256), 2),
+    (dict(q=FAKE + 8), 3), (dict(v=FAKE + 2), 3), (dict(lse=FAKE + 2), 3),
+])
+def test_fwd_rejects_invalid_arguments(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _dec(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, d=128, Lcap=256,
+             scale=0.1, S=4, ws=FAKE, wsb=None, stream=None)
+    a.update(kw)
+    if a["wsb"] is None:
+        a["wsb"] = lib.attn_decode_workspace_size(a["B"], a["Hq"], a["d"], max(a["S"], 1))
+    return lib.attn_decode(a["q"], a["kc"], a["vc"], a["sl"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                           a["d"], a["Lcap"], a["scale"], a["S"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(sl=None), 1), (dict(Hq=6, Hkv=4), 1), (dict(S=0), 1),
+    (dict(S=17), 1), (dict(Lcap=0), 1), (dict(scale=-1.0), 1), (dict(d=80), 2),
+    (dict(Hq=18, Hkv=2), 2), (dict(kc=FAKE + 4), 3), (dict(sl=FAKE + 2), 3),
+    (dict(ws=None), 4), (dict(wsb=16), 4), (dict(ws=FAKE + 8), 3),
+])
+def test_decode_rejects_invalid_arguments(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, FAKE, FAKE, 4, 1024, 1e-6), 1), ((FAKE, FAKE, FAKE, 0, 1024, 1e-6), 1),
+    ((FAKE, FAKE, FAKE, 4, 1020, 1e-6), 1), ((FAKE, FAKE, FAKE, 4, 1024, -1.0), 1),
+    ((FAKE, FAKE, FAKE, 4, 16384, 1e-6), 2), ((FAKE + 4, FAKE, FAKE, 4, 1024, 1e-6), 3),
+])
+def test_rmsnorm_rejects_invalid_arguments(lib, args, code):
+    assert lib.rmsnorm_fwd(*args, None) == code
+
+
+def test_selftest_rejects_out_of_range_bound(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == 1
+    assert lib.attn_selftest_wait_timeout(2_000_000, None) == 1
+
+
+def test_rejected_calls_launch_nothing(lib):
+    n0 = lib.attn_kernel_launches()
+    _fwd(lib, d=96)
+    _dec(lib, S=0)
+    lib.rmsnorm_fwd(None, FAKE, FAKE, 4, 1024, 1e-6, None)
+    assert lib.attn_kernel_launches() == n0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import exact_tiled_attention_attn_gb300 as attn
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        attn.rmsnorm(x, torch.ones(64, dtype=torch.bfloat16))

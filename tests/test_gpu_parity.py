@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle at sizes
+the oracle finishes in seconds: several tiles, ragged tails, the degenerate
+cases, both head dims, every grouping mode of the prefill kernel, and the
+split-count range of flash-decoding."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_common import assert_attn_close, assert_norm_close, f64, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    return require_gpu()
+
+
+DEV = "cuda"
+
+
+def _prefill_case(attn, B, Hq, Hkv, Tq, Tk, d, causal, seed, q_scale=1.0, scale=None):
+    q, k, v = W.attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed, q_scale=q_scale)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    O, L = oracle.attention(f64(q), f64(k), f64(v), causal, scale)
+    return o, lse, O, L
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def test_single_head_workload_fp32_inputs(attn):
+    # 1 x 1 x 256 x 64 causal, fp32 N(0,1) inputs rounded once to bf16
+    shp = W.SINGLE_HEAD
+    q, k, v, (q32, k32, v32) = W.attention_inputs(shp)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=shp.scale)
+    torch.cuda.synchronize()
+    O, L = oracle.attention(f64(q), f64(k), f64(v), True, shp.scale)
+    assert_attn_close(o, lse, O, L, "single head")
+    # information only: distance to the oracle on the unrounded fp32 inputs
+    O32, _ = oracle.attention(f64(q32), f64(k32), f64(v32), True, shp.scale)
+    print("max |O - O*(fp32 inputs)| =", np.abs(f64(o) - O32).max())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2), (8, 2), (6, 2), (3, 1)])
+def test_prefill_grouping_modes(attn, d, causal, Hq, Hkv):
+    # g = 1, 2, 4 (pairs of heads) and g = 3 (pairs of row tiles); T spans 3 tiles + a ragged tail
+    o, lse, O, L = _prefill_case(attn, 2, Hq, Hkv, 300, 300, d, causal, seed=100 + Hq + d)
+    assert_attn_close(o, lse, O, L, f"B2 Hq{Hq} Hkv{Hkv} d{d} causal{causal}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 255, 256, 257, 640])
+def test_prefill_lengths_and_tails(attn, T):
+    for causal in (False, True):
+        o, lse, O, L = _prefill_case(attn, 1, 2, 1, T, T, 128, causal, seed=200 + T)
+        assert_attn_close(o, lse, O, L, f"T{T} causal{causal}")
+
+
+@pytest.mark.parametrize("Tq,Tk", [(100, 300), (300, 100), (1, 513), (513, 1), (128, 384)])
+def test_prefill_rectangular(attn, Tq, Tk):
+    for causal in (False, True):
+        o, lse, O, L = _prefill_case(attn, 1, 4, 2, Tq, Tk, 64, causal, seed=300 + Tq + Tk)
+        assert_attn_close(o, lse, O, L, f"Tq{Tq} Tk{Tk} causal{causal}")
+
+
+def test_prefill_single_key_returns_its_value(attn):
+    o, lse, O, L = _prefill_case(attn, 1, 4, 4, 5, 1, 128, False, seed=5)
+    assert_attn_close(o, lse, O, L, "Tk=1")
+    q, k, v = W.attention_inputs_custom(1, 4, 4, 5, 1, 128, 5)
+    # every row must return v_0 exactly (rounded to bf16, which v already is)
+    assert torch.equal(o.cpu(), v.expand(1, 4, 5, 128))
+
+
+def test_prefill_causal_row0_is_v0(attn):
+    q, k, v = W.attention_inputs_custom(1, 4, 2, 256, 256, 128, 9)
+    o, _ = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    vv = v.repeat_interleave(2, dim=1)
+    assert torch.equal(o[:, :, 0].cpu(), vv[:, :, 0])
+
+
+def test_prefill_constant_values(attn):
+    q, k, _ = W.attention_inputs_custom(1, 2, 1, 300, 300, 64, 10)
+    v = torch.full((1, 1, 300, 64), 0.8125, dtype=torch.bfloat16)
+    o, _ = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    # P is rounded to bf16 for the P.V product while l sums the fp32 P, so the
+    # constant comes back within one bf16 ulp (2^-8 at 0.8125), not bit-exactly
+    assert (o.float().cpu() - 0.8125).abs().max() <= 2 ** -8
+
+
+def test_prefill_zero_queries_mean_and_log_count(attn):
+    q = torch.zeros(1, 2, 260, 128, dtype=torch.bfloat16)
+    _, k, v = W.attention_inputs_custom(1, 2, 2, 260, 260, 128, 11)
+    for causal in (False, True):
+        o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+        torch.cuda.synchronize()
+        n = np.arange(1, 261) if causal else np.full(260, 260)
+        assert np.abs(f64(lse)[0] - np.log(n)[None, :]).max() <= 1e-3
+        O, L = oracle.attention(f64(q), f64(k), f64(v), causal, 1 / math.sqrt(128))
+        assert_attn_close(o, lse, O, L, f"zero q causal{causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_peaked_scores(attn, causal):
+    # q scaled by 100: nearly one-hot rows, the max moves a lot between blocks
+    o, lse, O, L = _prefill_case(attn, 1, 2, 1, 384, 384, 64, causal, seed=12, q_scale=100.0)
+    assert_attn_close(o, lse, O, L, f"peaked causal{causal}")
+
+
+def test_prefill_increasing_scores_force_rescales(attn):
+    # keys grow along the sequence so every block raises the row maximum by a lot
+    d, T = 64, 640
+    q = torch.ones(1, 1, T, d, dtype=torch.bfloat16)
+    k = (torch.arange(T, dtype=torch.float32)[:, None] / 16.0).expand(T, d).reshape(1, 1, T, d).to(torch.bfloat16)
+    _, _, v = W.attention_inputs_custom(1, 1, 1, T, T, d, 13)
+    scale = 1.0 / d
+    for causal in (False, True):
+        o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+        torch.cuda.synchronize()
+        O, L = oracle.attention(f64(q), f64(k), f64(v), causal, scale)
+        assert_attn_close(o, lse, O, L, f"rescale causal{causal}")
+
+
+def test_prefill_custom_scale_and_no_lse(attn):
+    q, k, v = W.attention_inputs_custom(2, 4, 4, 200, 200, 64, 14)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=False, scale=0.37, return_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    O, _ = oracle.attention(f64(q), f64(k), f64(v), False, 0.37)
+    assert_attn_close(o, None, O, None, "scale 0.37")
+
+
+def test_prefill_does_not_touch_inputs_or_outside_output(attn):
+    q, k, v = W.attention_inputs_custom(1, 2, 1, 200, 200, 128, 15)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    flat = torch.full((2 * 200 * 128 + 2 * 4096,), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = flat[4096:4096 + 2 * 200 * 128].view(1, 2, 200, 128)
+    lse_flat = torch.full((400 + 2048,), 7.0, dtype=torch.float32, device=DEV)
+    lse = lse_flat[1024:1424].view(1, 2, 200)
+    attn.fwd(qd, kd, vd, causal=True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(flat[:4096] == 7.0) and torch.all(flat[4096 + 2 * 200 * 128:] == 7.0)
+    assert torch.all(lse_flat[:1024] == 7.0) and torch.all(lse_flat[1424:] == 7.0)
+    assert torch.equal(qd.cpu(), q) and torch.equal(kd.cpu(), k) and torch.equal(vd.cpu(), v)
+
+
+def test_prefill_deterministic(attn):
+    q, k, v = W.attention_inputs_custom(1, 4, 2, 700, 700, 128, 16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1, l1 = attn.fwd(qd, kd, vd, causal=True)
+    o2, l2 = attn.fwd(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------- decode
+
+def _decode_case(attn, B, Hq, Hkv, d, Lcap, lens, splits, seed):
+    shp = W.DecodeShape("t", B, Hq, Hkv, d, 1, Lcap, seed)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=lens)
+    qd, kd, vd, sd = q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV)
+    O, L = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), shp.scale)
+    outs = []
+    for S in splits:
+        o, lse = attn.decode(qd, kd, vd, sd, num_splits=S)
+        torch.cuda.synchronize()
+        assert_attn_close(o, lse, O, L, f"decode B{B} Hq{Hq} Hkv{Hkv} d{d} S{S}")
+        outs.append((o, lse))
+    return outs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (8, 1), (6, 2), (16, 2)])
+def test_decode_groupings(attn, d, Hq, Hkv):
+    _decode_case(attn, 3, Hq, Hkv, d, 300, [1, 77, 300], [1, 4, 19], seed=400 + Hq + d)
+
+
+def test_decode_split_range_and_lengths(attn):
+    lens = [1, 15, 16, 17, 31, 32, 33, 1000, 4095, 4096]
+    Lcap = 4096
+    _decode_case(attn, len(lens), 8, 2, 128, Lcap, lens, [1, 2, 3, 8, 64, 255, 256], seed=500)
+
+
+def test_decode_equals_prefill_last_row(attn):
+    # decode of the last token == row L-1 of causal prefill over the same keys
+    L = 333
+    q, k, v = W.attention_inputs_custom(1, 8, 2, L, L, 128, 17)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o_p, l_p = attn.fwd(qd, kd, vd, causal=True)
+    sl = torch.tensor([L], dtype=torch.int32, device=DEV)
+    o_d, l_d = attn.decode(qd[:, :, L - 1].contiguous(), kd, vd, sl, num_splits=5)
+    torch.cuda.synchronize()
+    assert np.abs(f64(o_p[:, :, L - 1]) - f64(o_d)).max() <= 2e-2
+    assert np.abs(f64(l_p[:, :, L - 1]) - f64(l_d)).max() <= 1e-3
+
+
+def test_decode_deterministic_for_fixed_splits(attn):
+    shp = W.DecodeShape("t", 4, 8, 2, 128, 1, 2000, 18)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=[2000, 5, 999, 1500])
+    args = (q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV))
+    a = attn.decode(*args, num_splits=7)
+    b = attn.decode(*args, num_splits=7)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_decode_out_of_range_lengths_are_defined(attn):
+    # precondition is 1 <= L <= Lcap; outside it the kernel clamps (<= 0: O = 0, LSE = -inf)
+    shp = W.DecodeShape("t", 3, 4, 2, 64, 1, 64, 19)
+    q, kc, vc, _ = W.decode_inputs(shp, seqlens=[64, 64, 64])
+    sl = torch.tensor([0, -5, 500], dtype=torch.int32)
+    o, lse = attn.decode(q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV), num_splits=2)
+    torch.cuda.synchronize()
+    assert torch.all(o[:2].cpu() == 0) and torch.all(torch.isneginf(lse[:2].cpu()))
+    O, L = oracle.decode(f64(q[2:]), f64(kc[2:]), f64(vc[2:]), [64], shp.scale)
+    assert_attn_close(o[2:], lse[2:], O, L, "clamped length")
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+
+@pytest.mark.parametrize("T,D", [(1, 8), (37, 64), (300, 1000), (4096, 1024), (33, 4096), (5, 8192), (17, 2056)])
+def test_rmsnorm_shapes(attn, T, D):
+    gen = torch.Generator().manual_seed(T * 31 + D)
+    x = torch.randn(T, D, generator=gen).to(torch.bfloat16)
+    w = (0.5 + torch.rand(D, generator=gen)).to(torch.bfloat16)
+    y = attn.rmsnorm(x.to(DEV), w.to(DEV), eps=1e-6)
+    torch.cuda.synchronize()
+    assert_norm_close(y, oracle.rmsnorm(f64(x), f64(w), 1e-6), f"T{T} D{D}")
+
+
+def test_rmsnorm_workload_full(attn):
+    x, w = W.norm_inputs(W.NORM_QWEN)
+    xd = x.to(DEV)
+    y = attn.rmsnorm(xd, w.to(DEV), eps=W.NORM_QWEN.eps)
+    torch.cuda.synchronize()
+    assert_norm_close(y, oracle.rmsnorm(f64(x), f64(w), W.NORM_QWEN.eps), "X[4096,1024]")
+    assert torch.equal(xd.cpu(), x)
+
+
+def test_rmsnorm_special_inputs(attn):
+    D = 1024
+    x = torch.zeros(4, D, dtype=torch.bfloat16)
+    x[1] = 1.0
+    x[2, 0] = 1000.0
+    x[3] = 1e-3
+    w = torch.ones(D, dtype=torch.bfloat16)
+    y = attn.rmsnorm(x.to(DEV), w.to(DEV), eps=1e-6).cpu()
+    assert torch.all(y[0] == 0)
+    assert torch.all(torch.isfinite(y))
+    assert_norm_close(y, oracle.rmsnorm(f64(x), f64(w), 1e-6), "special")
+    # unit weight: per-row RMS of the output ~ 1
+    gen = torch.Generator().manual_seed(3)
+    xr = torch.randn(16, D, generator=gen).to(torch.bfloat16)
+    yr = f64(attn.rmsnorm(xr.to(DEV), w.to(DEV), eps=1e-6))
+    assert np.abs(np.sqrt((yr ** 2).mean(axis=1)) - 1).max() < 1e-2
+
+
+# ----------------------------------------------------------------------------- failure path
+
+def test_bounded_wait_reports_timeout_and_context_survives(attn):
+    assert attn.last_device_error() == 0
+    attn.selftest_wait_timeout(2000)
+    assert attn.last_device_error() == 6  # ATTN_ERR_TIMEOUT
+    assert attn.last_device_error() == 0  # cleared
+    # the context still works afterwards
+    x = torch.ones(8, 64, dtype=torch.bfloat16, device=DEV)
+    y = attn.rmsnorm(x, torch.ones(64, dtype=torch.bfloat16, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.allclose(y.float().cpu(), torch.ones(8, 64), atol=1e-2)
