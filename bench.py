@@ -1,0 +1,429 @@
+"""Benchmark of the exact tiled attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs:
+  1. fused RMSNorm on X[4096, 1024] (bf16, eps 1e-6),
+  2. causal GQA prefill B=2, Hq=32, Hkv=8, T=8192, d=128 (bf16, scale 1/sqrt(128)),
+  3. flash-decoding B=16, Hq=32, Hkv=8, d=128 over a bf16 KV cache with
+     per-sequence lengths drawn uniformly in [8192, 32768] (split-KV + combine).
+All inputs are resident in HBM before the timed region. The headline value is
+the causal-prefill throughput in TFLOP/s (algorithmic FLOPs: 4d per visible
+query/key pair); the decode KV-stream GB/s and the RMSNorm GB/s are reported
+beside it. Kernel times come from CUDA events recorded on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --impl reference the float64 CPU oracle is timed instead, on a bounded
+sample of the same workload (the oracle is a deliberately slow definition, so
+this is a reported baseline, not a target).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "attention TFLOPS (causal prefill) & decode KV-stream GB/s, as % of GB300 roofline"
+PREFILL = W.GQA_LLAMA
+DECODE = W.DECODE_LLAMA
+NORM = W.NORM_QWEN
+WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms in a subprocess."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index_or_uuid):
+        self.dev = device_index_or_uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        """Stop sampling; summarise the samples that arrived between t0 and t1 (wall time)."""
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def _dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import exact_tiled_attention_attn_gb300 as attn
+    from exact_tiled_attention_attn_gb300.build import build
+
+    world, rank, local = _dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build()
+    attn.lib()
+
+    # ---- inputs (seeded, generated on the host, copied once to HBM)
+    q, k, v = W.attention_inputs(PREFILL)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty(PREFILL.B, PREFILL.Hq, PREFILL.T, dtype=torch.float32, device=dev)
+    x, w = W.norm_inputs(NORM)
+    xd, wd = x.to(dev), w.to(dev)
+    yd = torch.empty_like(xd)
+    dq, dkc, dvc, dsl = W.decode_inputs(DECODE)
+    dqd, dkcd, dvcd, dsld = dq.to(dev), dkc.to(dev), dvc.to(dev), dsl.to(dev)
+    del dkc, dvc
+    splits = args.splits or attn.default_splits(DECODE.B, DECODE.Hkv, DECODE.Lcap)
+    ws = torch.empty(attn.decode_workspace_size(DECODE.B, DECODE.Hq, DECODE.d, splits), dtype=torch.uint8,
+                     device=dev)
+    dod = torch.empty_like(dqd)
+    dlse = torch.empty(DECODE.B, DECODE.Hq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        attn.rmsnorm(xd, wd, eps=NORM.eps, out=yd)
+        if ev is not None:
+            ev[1].record(stream)
+        attn.fwd(qd, kd, vd, causal=True, scale=PREFILL.scale, out=od, lse=lsed)
+        if ev is not None:
+            ev[2].record(stream)
+        attn.decode(dqd, dkcd, dvcd, dsld, scale=DECODE.scale, num_splits=splits, workspace=ws, out=dod,
+                    lse=dlse)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid if uuid else local)
+    sampler.start()
+    time.sleep(0.4)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = attn.kernel_launches()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    launches = attn.kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(wall0, wall1)
+    assert attn.last_device_error() == 0
+
+    total_ms = t_start.elapsed_time(t_end)
+    norm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if world > 1:
+        t = torch.tensor([total_ms, fwd_ms, dec_ms, norm_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, fwd_ms, dec_ms, norm_ms = [float(a) for a in t.tolist()]
+
+    peaks = _peaks()
+    flops = PREFILL.flops()
+    sum_l = int(dsl.sum().item())
+    dec_bytes = (4 * DECODE.Hkv * DECODE.d * sum_l + 2 * DECODE.B * DECODE.Hq * DECODE.d * 2
+                 + DECODE.B * DECODE.Hq * 4 + DECODE.B * 4)
+    norm_bytes = NORM.hbm_bytes()
+    prefill_tflops = flops / (fwd_ms * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9
+    value = world * prefill_tflops
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
+        qd2, kd2, vd2 = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+
+        def e2e_step():
+            qd2.copy_(qh, non_blocking=True)
+            kd2.copy_(kh, non_blocking=True)
+            vd2.copy_(vh, non_blocking=True)
+            o2, l2 = attn.fwd(qd2, kd2, vd2, causal=True, scale=PREFILL.scale, out=od, lse=lsed)
+            oh.copy_(o2, non_blocking=True)
+            lh.copy_(l2, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        h2d = (q.numel() + k.numel() + v.numel()) * 2
+        d2h = q.numel() * 2 + lsed.numel() * 4
+        e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_heads)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16; decode lengths ~U[8192,32768] seed 1004)",
+            "config": {"workload": WORKLOAD, "prefill_ms": round(fwd_ms, 4), "decode_ms": round(dec_ms, 4),
+                       "rmsnorm_ms": round(norm_ms, 4), "decode_num_splits": splits,
+                       "decode_sum_lengths": sum_l,
+                       "l2": "inputs larger than L2: prefill reads 201 MB, decode streams "
+                             f"{dec_bytes / 1e9:.2f} GB between reuses of any buffer",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128>",
+                         "achieved": round(prefill_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": round(prefill_tflops / peaks["bf16"], 4), "traffic": args.traffic,
+                         "peak_source": f"{peaks['source']} bf16 (burst)",
+                         "flops_per_launch": flops},
+            "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
+                       "frac": round(dec_gbs / peaks["hbm"], 4), "bytes_per_launch": dec_bytes,
+                       "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>"},
+            "rmsnorm": {"value": round(norm_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
+                        "frac": round(norm_gbs / peaks["hbm"], 4), "bytes_per_launch": norm_bytes},
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs():
+    """float64 copies of the prefill workload's inputs (generated once per process)."""
+    if not _ORACLE_INPUTS:
+        q, k, v = W.attention_inputs(PREFILL)
+        _ORACLE_INPUTS.update(q=q, k=k, v=v)
+    return _ORACLE_INPUTS["q"], _ORACLE_INPUTS["k"], _ORACLE_INPUTS["v"]
+
+
+def _oracle_sample(heads):
+    """The oracle on every query row of the given (batch, head) pairs of the prefill workload.
+
+    Returns (flops, seconds); only the oracle call is timed.
+    """
+    import oracle
+    q, k, v = _oracle_inputs()
+    g = PREFILL.Hq // PREFILL.Hkv
+    T = PREFILL.T
+    rows = np.arange(T)
+    flops, dt = 0.0, 0.0
+    for b, h in heads:
+        qh = W.to_f64(q[b, h])[None, None]
+        kh = W.to_f64(k[b, h // g])[None, None]
+        vh = W.to_f64(v[b, h // g])[None, None]
+        t0 = time.perf_counter()
+        oracle.attention_rows(qh, kh, vh, 0, 0, rows, True, PREFILL.scale)
+        dt += time.perf_counter() - t0
+        flops += 4.0 * PREFILL.d * T * (T + 1) / 2
+    return flops, dt
+
+
+def cpu_baseline(n_heads: int):
+    heads = [(0, h) for h in range(n_heads)]
+    flops, dt = _oracle_sample(heads)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 three-pass oracle on all {PREFILL.T} causal query rows of {n_heads} of the "
+                      f"{PREFILL.B * PREFILL.Hq} (batch, head) pairs of the prefill workload (d={PREFILL.d}); "
+                      f"{flops / 1e9:.1f} GFLOP in {dt:.2f} s; numpy BLAS with its default threads "
+                      "(all host cores)"}
+
+
+def _oracle_rows(b: int, h: int, rows: int):
+    """The oracle on the last `rows` causal query rows of one (batch, head) pair. Returns (flops, s)."""
+    import oracle
+    q, k, v = _oracle_inputs()
+    g = PREFILL.Hq // PREFILL.Hkv
+    T = PREFILL.T
+    sel = np.arange(T - rows, T)
+    qh = W.to_f64(q[b, h])[None, None]
+    kh = W.to_f64(k[b, h // g])[None, None]
+    vh = W.to_f64(v[b, h // g])[None, None]
+    t0 = time.perf_counter()
+    oracle.attention_rows(qh, kh, vh, 0, 0, sel, True, PREFILL.scale)
+    return 4.0 * PREFILL.d * float(np.sum(sel + 1)), time.perf_counter() - t0
+
+
+def run_reference(args):
+    world, rank, _ = _dist_setup()
+    if rank != 0:
+        return
+    _oracle_inputs()
+    # Size each step's sample so the whole run stays near --ref-seconds of oracle time.
+    _, t_cal = _oracle_rows(0, 0, 256)
+    per_step = args.ref_seconds / (args.steps + args.warmup)
+    rows = int(max(16, min(PREFILL.T, 256 * per_step / max(t_cal, 1e-6))))
+    for i in range(args.warmup):
+        _oracle_rows(0, i % PREFILL.Hq, rows)
+    tot_f, tot_t = 0.0, 0.0
+    for i in range(args.steps):
+        f, t = _oracle_rows(i // PREFILL.Hq % PREFILL.B, i % PREFILL.Hq, rows)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: float64 three-pass oracle on the last {rows} causal query rows (of {PREFILL.T}) of one "
+              "(batch, head) pair of the prefill workload; numpy BLAS with its default threads")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 decoded to float64)",
+        "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = library default)")
+    ap.add_argument("--cpu-heads", type=int, default=8, help="(batch, head) pairs in the CPU-baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="approximate oracle time of a whole --impl reference run")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per prefill launch from an ncu capture, if known for this build")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,97 @@
+"""Run one operation of the library on a named synthetic workload, a few times.
+
+A small driver for profilers and quick timing: it allocates only what the
+chosen operation needs, runs it ``--iters`` times on cuda:0 and prints the
+mean CUDA-event time of the launches after the first.
+
+  python -m exact_tiled_attention_attn_gb300.run_op --op prefill --workload gqa-llama --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op decode --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op rmsnorm --iters 3
+
+Workloads (seeded N(0,1) bf16 inputs):
+  single-head  causal 1 x 1 x 256 x 64
+  mha-gpt2     non-causal B8 H12 T4096 d64
+  gqa-qwen     causal B1 Hq16 Hkv8 T4096 d128
+  gqa-llama    causal B2 Hq32 Hkv8 T8192 d128 (default for prefill)
+  decode-llama B16 Hq32 Hkv8 d128, lengths ~U[8192, 32768] (decode)
+  norm-qwen    X[4096, 1024] (rmsnorm)
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PREFILL_WORKLOADS = {"single-head": "SINGLE_HEAD", "mha-gpt2": "MHA_GPT2", "gqa-qwen": "GQA_QWEN",
+                     "gqa-llama": "GQA_LLAMA"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--op", choices=["prefill", "decode", "rmsnorm"], required=True)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--splits", type=int, default=0)
+    args = ap.parse_args(argv)
+
+    import torch
+    import workloads as W
+    import exact_tiled_attention_attn_gb300 as attn
+    from exact_tiled_attention_attn_gb300.build import build
+
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.op == "prefill":
+        shp = getattr(W, PREFILL_WORKLOADS[args.workload or "gqa-llama"])
+        q, k, v = W.attention_inputs(shp)[:3]
+        q, k, v = q.to(dev), k.to(dev), v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+        def run():
+            attn.fwd(q, k, v, causal=shp.causal, scale=shp.scale, out=o, lse=lse)
+        work, unit = shp.flops() / 1e12, "TFLOP/s"
+    elif args.op == "decode":
+        shp = W.DECODE_LLAMA
+        q, kc, vc, sl = W.decode_inputs(shp)
+        q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
+        S = args.splits or attn.default_splits(shp.B, shp.Hkv, shp.Lcap)
+        ws = torch.empty(attn.decode_workspace_size(shp.B, shp.Hq, shp.d, S), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(shp.B, shp.Hq, dtype=torch.float32, device=dev)
+
+        def run():
+            attn.decode(q, kc, vc, sld, scale=shp.scale, num_splits=S, workspace=ws, out=o, lse=lse)
+        work, unit = 4 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (KV stream)"
+    else:
+        shp = W.NORM_QWEN
+        x, w = W.norm_inputs(shp)
+        x, w = x.to(dev), w.to(dev)
+        y = torch.empty_like(x)
+
+        def run():
+            attn.rmsnorm(x, w, eps=shp.eps, out=y)
+        work, unit = shp.hbm_bytes() / 1e9, "GB/s"
+
+    run()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    n = max(1, args.iters - 1)
+    ev[0].record()
+    for _ in range(n):
+        run()
+    ev[1].record()
+    torch.cuda.synchronize()
+    status = attn.last_device_error()
+    ms = ev[0].elapsed_time(ev[1]) / n
+    print(f"{args.op} {shp.name}: {ms:.4f} ms/launch, {work / (ms * 1e-3):.1f} {unit}, device status {status}")
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
