@@ -18,7 +18,7 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "decode", "rmsnorm", "decode_workspace_size", "default_splits",
+__all__ = ["fwd", "decode", "decode_noalloc", "rmsnorm", "decode_workspace_size", "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
 
 
@@ -113,6 +113,42 @@ def decode(q, kcache, vcache, seqlens, scale: float | None = None, num_splits: i
                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream))
     _lib.check("attn_decode", st)
+    return out, lse
+
+
+def decode_noalloc(q, kcache, vcache, seqlens, scale: float | None = None, num_splits: int | None = None,
+                   out=None, lse=None, return_lse: bool = True, stream=None):
+    """``decode`` without a workspace: the split partials go to the library's fixed
+    32 MiB device array, so the library itself allocates nothing.
+
+    For callers that cannot allocate device memory at decode time (a KV-cache pool
+    that owns the memory, an allocation budget, no allocation allowed mid-step).
+    ``out`` and ``lse`` must then be passed in as well. All such calls share the one
+    array: calls that can overlap on the GPU must be serialised by the caller. The
+    first call on a device looks the array up and should come before any stream
+    capture. Raises AttnError (ATTN_ERR_WORKSPACE) when the partials for
+    ``num_splits`` would not fit in 32 MiB.
+    """
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("kcache", kcache, torch.bfloat16, 4)
+    _check_tensor("vcache", vcache, torch.bfloat16, 4)
+    _check_tensor("seqlens", seqlens, torch.int32, 1)
+    B, Hq, d = q.shape
+    Hkv, Lcap = kcache.shape[1], kcache.shape[2]
+    if kcache.shape != vcache.shape or kcache.shape[0] != B or kcache.shape[3] != d:
+        raise ValueError("kcache and vcache must both be [B, Hkv, Lcap, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        num_splits = default_splits(B, Hkv, Lcap)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_decode_noalloc(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), seqlens.data_ptr(),
+                                         out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                         B, Hq, Hkv, d, Lcap, float(scale), int(num_splits), _stream_ptr(stream))
+    _lib.check("attn_decode_noalloc", st)
     return out, lse
 
 

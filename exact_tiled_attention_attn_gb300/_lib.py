@@ -29,6 +29,7 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode_default_splits": (_I, [_I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t, _P]),
+    "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "rmsnorm_fwd": (_I, [_P, _P, _P, _I, _I, _F, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_device_error": (_I, [_P]),

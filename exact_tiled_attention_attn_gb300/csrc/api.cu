@@ -14,6 +14,8 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
                           int B, int Hq, int Hkv, int d, int Lcap, float scale, int S, int C, void* workspace,
                           cudaStream_t stream, int* launched);
 cudaError_t launch_rmsnorm(const void* x, const void* w, void* y, int T, int D, float eps, cudaStream_t s);
+size_t decode_noalloc_capacity();
+cudaError_t decode_noalloc_scratch(void** ptr);
 uint32_t prefill_take_device_error();
 uint32_t decode_take_device_error();
 uint32_t rmsnorm_take_device_error();
@@ -105,6 +107,34 @@ attn_status attn_decode(const void* q, const void* kcache, const void* vcache, c
   int launched = 0;
   const cudaError_t err = launch_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits,
                                         C, workspace, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                                void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap, float scale,
+                                int num_splits, cudaStream_t stream) {
+  if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  // The partials must fit the library's fixed scratch; refuse before touching the device.
+  if (attn_decode_workspace_size(B, Hq, d, num_splits) > decode_noalloc_capacity()) return ATTN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (decode_noalloc_scratch(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int C = decode_chunk(Lcap, num_splits);
+  int launched = 0;
+  const cudaError_t err = launch_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits,
+                                        C, scratch, stream, &launched);
   g_launches.fetch_add(static_cast<unsigned long long>(launched));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -21,6 +21,8 @@
 //
 // Scores are kept in the base-2 domain: q is pre-multiplied by
 // c = scale * log2(e), so p = 2^(c*s - m); LSE = (m + log2 l) * ln 2.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace gb300 {
@@ -373,5 +375,50 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
 }
 
 uint32_t decode_take_device_error() { return take_device_error_word(); }
+
+// ---------------------------------------------------------------------------------------
+// Fixed scratch for attn_decode_noalloc.
+//
+// Some callers cannot allocate device memory at the moment they want to decode: an
+// engine that has already handed (nearly) all of HBM to its KV-cache pool, code running
+// under a custom allocator or a memory budget that forbids new allocations, or a caller
+// that must not trigger an allocation (and the synchronisation cudaMalloc/cudaFree can
+// imply) in the middle of its step. For them the split partials live in this file-scope
+// device array instead of a caller-provided workspace. It is part of the module image:
+// every GPU that loads this library holds these bytes until the process exits.
+// Nothing in it needs to start at zero: each call's split kernel writes every partial
+// that the same call's combine kernel reads. All calls share it, so two such calls that
+// can run at the same time on the GPU (different streams, or different host threads)
+// race on it and must be serialised by the caller.
+// ---------------------------------------------------------------------------------------
+constexpr size_t kDecodeNoAllocScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeNoAllocScratchBytes];
+
+size_t decode_noalloc_capacity() { return kDecodeNoAllocScratchBytes; }
+
+// Device address of g_decode_scratch on the current device. In host code the symbol is
+// only a host-side stand-in, so its device address is looked up once per device (with
+// that device current) and cached. The first lookup on a device may load this library's
+// device code there; it does not call cudaMalloc.
+cudaError_t decode_noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (err != cudaSuccess) return err;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 }  // namespace gb300

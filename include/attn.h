@@ -127,6 +127,37 @@ attn_status attn_decode(const void* q, const void* kcache, const void* vcache,
                         cudaStream_t stream);
 
 /*
+ * attn_decode_noalloc - attn_decode for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot provide attn_decode's workspace: an engine whose KV-cache
+ * pool already owns (nearly) all device memory, code running under an allocator
+ * or memory budget that forbids new allocations, or a step that must not call
+ * cudaMalloc/cudaFree (and the synchronisation they can imply) while it runs.
+ * It computes exactly what attn_decode computes, with the same kernels, and takes
+ * the same arguments except the workspace: the per-split partials go to a fixed
+ * device array inside the library (32 MiB, 256-byte aligned). That array is part
+ * of the library's device image, so every GPU that loads the library holds the
+ * 32 MiB until the process exits. This call never calls cudaMalloc, cudaFree or
+ * any allocating library routine.
+ *
+ *   Size limit: attn_decode_workspace_size(B, Hq, d, num_splits) must be
+ *   <= 32 MiB (33554432 bytes); larger requests return ATTN_ERR_WORKSPACE before
+ *   anything runs (use fewer splits, or attn_decode with your own workspace).
+ *   First call on a device: it looks up the array's device address on the
+ *   current device (cudaGetSymbolAddress) and caches it; make that first call
+ *   before any stream capture on that device.
+ *   Sharing: every call uses the same array, which keeps the previous call's
+ *   contents (nothing in it needs to start at zero). Calls that can overlap on
+ *   the GPU (other streams, other host threads) race on it: serialise them.
+ * Other arguments, layouts, alignment and errors: as attn_decode.
+ */
+attn_status attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                                const int* seqlens, void* o, float* lse,
+                                int B, int Hq, int Hkv, int d, int Lcap, float scale,
+                                int num_splits, cudaStream_t stream);
+
+/*
  * rmsnorm_fwd - y = x / sqrt(mean_j x_j^2 + eps) * w for every row, one pass.
  *
  * Defined by: "Module 07: Fused operators and FlashAttention", section
