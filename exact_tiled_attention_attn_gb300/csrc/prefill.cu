@@ -202,53 +202,68 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------ MMA issuer ------------------------------
+    // Issue order per key block j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The tensor pipe
+    // runs one thread's MMAs in issue order, so S_q(j) may overwrite the TMEM columns
+    // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
+    // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
     if (lane == 0) {
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
       bool ok = mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
       tc_fence_after();
       bool any_mma = false;
-      for (int j = 0; ok && j < n_iter; ++j) {
-        const int s = j % Cfg::kStages;
-        const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
-        if (!(ok = mbar_wait(&k_full[s], ph, abort_p, kPrefillWaitTimeoutNs))) break;
-        tc_fence_after();
-        for (int q = 0; q < 2 && ok; ++q) {
-          if (j >= u.nkv[q]) continue;
-          if (j > 0) {  // PV of the previous block read P from these columns
-            if (!(ok = mbar_wait(&o_done[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
+      for (int j = 0; ok && j <= n_iter; ++j) {
+        const bool do_s = j < n_iter;  // S(j) = Q K(j)^T
+        const bool do_pv = j > 0;      // O += P(j-1) V(j-1)
+        const int sk = j % Cfg::kStages;
+        const uint32_t phk = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
+        const int sv = (j - 1 + Cfg::kStages) % Cfg::kStages;
+        const uint32_t phv = static_cast<uint32_t>((j - 1) / Cfg::kStages) & 1u;
+        bool k_ready = false;
+        if (do_pv) {
+          if (!(ok = mbar_wait(&v_full[sv], phv, abort_p, kPrefillWaitTimeoutNs))) break;
+          tc_fence_after();
+        }
+        for (int q = 0; q < 2; ++q) {
+          const int nkv_q = q ? u.nkv[1] : u.nkv[0];
+          if (do_pv && j - 1 < nkv_q) {
+            if (!(ok = mbar_wait(&p_full[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
               break;
             tc_fence_after();
-          }
-          const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+            const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
+            const uint32_t a_p = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
-            const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
-            const uint64_t db = make_sdesc_sw128(sKa + s * Cfg::kTileBytes + off, 16, 1024);
-            umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 128 / 16; ++kk) {
+              const uint64_t db = make_sdesc_sw128(sVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
+              umma_ts(d_o, a_p + kk * 8, db, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&o_done[q]);
           }
-          any_mma = true;
-          umma_commit(&s_full[q]);
+          if (do_s && j < nkv_q) {
+            if (!k_ready) {
+              if (!(ok = mbar_wait(&k_full[sk], phk, abort_p, kPrefillWaitTimeoutNs))) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
+              const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
+              const uint64_t db = make_sdesc_sw128(sKa + sk * Cfg::kTileBytes + off, 16, 1024);
+              umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            any_mma = true;
+            umma_commit(&s_full[q]);
+          }
         }
         if (!ok) break;
-        umma_commit(&k_empty[s]);
-        if (!(ok = mbar_wait(&v_full[s], ph, abort_p, kPrefillWaitTimeoutNs))) break;
-        tc_fence_after();
-        for (int q = 0; q < 2 && ok; ++q) {
-          if (j >= u.nkv[q]) continue;
-          if (!(ok = mbar_wait(&p_full[q], static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
-          tc_fence_after();
-          const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
-          const uint32_t a_p = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
-#pragma unroll
-          for (int kk = 0; kk < 128 / 16; ++kk) {
-            const uint64_t db = make_sdesc_sw128(sVa + s * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
-            umma_ts(d_o, a_p + kk * 8, db, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        if (do_s) {
+          if (!k_ready) {  // neither tile needed K(j): still consume the stage in order
+            if (!(ok = mbar_wait(&k_full[sk], phk, abort_p, kPrefillWaitTimeoutNs))) break;
           }
-          umma_commit(&o_done[q]);
+          umma_commit(&k_empty[sk]);
         }
-        if (!ok) break;
-        umma_commit(&v_empty[s]);
+        if (do_pv) umma_commit(&v_empty[sv]);
       }
       if (any_mma) {  // every MMA has finished before TMEM is released
         umma_commit(&mma_drain);
@@ -286,14 +301,17 @@ __global__ void __launch_bounds__(320, 1)
         for (int k = 0; k < 128; ++k)
           if (j0 + k > lim) sr[k] = __float_as_uint(-INFINITY);
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      // row max over columns 0..127: 4 pairwise seeds, then 15 rounds of 3-input max
+      float mx0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
+      float mx1 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
+      float mx2 = fmaxf(__uint_as_float(sr[4]), __uint_as_float(sr[5]));
+      float mx3 = fmaxf(__uint_as_float(sr[6]), __uint_as_float(sr[7]));
 #pragma unroll
-      for (int k = 4; k < 128; k += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[k]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[k + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[k + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[k + 3]));
+      for (int k = 8; k < 128; k += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[k + 4]), __uint_as_float(sr[k + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[k + 6]), __uint_as_float(sr[k + 7]));
       }
       const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       const float m_cand = fmaxf(m_run, m_blk);
@@ -305,22 +323,26 @@ __global__ void __launch_bounds__(320, 1)
       }
       const float base = (m_run == -INFINITY) ? 0.f : m_run;
 
-      const float nb = -base;
-      float sum0 = 0.f, sum1 = 0.f;
+      // p = 2^(s*c - base): packed fp32x2 FMA, one ex2 per element, packed row sums
+      const float2 c2 = make_float2(c, c);
+      const float2 nb2 = make_float2(-base, -base);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc * 32 + 2 * k]), c, nb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[cc * 32 + 2 * k + 1]), c, nb));
-          sum0 += p0;
-          sum1 += p1;
-          pk[k] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sr[cc * 32 + 2 * k]), __uint_as_float(sr[cc * 32 + 2 * k + 1])), c2, nb2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[k & 3] = __fadd2_rn(acc[k & 3], pp);
+          pk[k] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st16(t_s + cc * 16, pk);
       }
-      l_run = l_run * corr + (sum0 + sum1);
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      l_run = l_run * corr + ((a01.x + a01.y) + (a23.x + a23.y));
       if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
         // O holds the sum up to block j-1 relative to the old base: wait for that PV, rescale in TMEM
         // (done after P is written so the registers of S are free).
