@@ -101,6 +101,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep until the phase completes
+// (or about `hint_ns` passes) instead of polling, which keeps waiting warps off the
+// issue slots and the shared-memory pipe.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Gives up after `timeout_ns` of wall time or as soon as `*abort` is set by
 // another thread; on its own timeout it sets `*abort` and the device error
@@ -109,15 +124,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) {
-        *abort = 1;
-        report_device_error(kErrTimeout);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      report_device_error(kErrTimeout);
+      return false;
     }
   }
 }

@@ -33,16 +33,19 @@ namespace gb300 {
 
 constexpr uint64_t kPrefillWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;                   // log2 of the allowed growth of p
+constexpr int kIterRing = 4;                                // per-iteration completion barriers in flight
 
 template <int D>
 struct PrefillCfg {
   static constexpr int kBM = 128;                  // query rows per tile
   static constexpr int kBN = 128;                  // keys per tile
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  // One ring of K/V slots: item 2j holds K(j), item 2j+1 holds V(j), slot = item % kSlots.
+  // An odd slot count lets V(j) reuse the slot of K(j-2), freed as soon as S(j-2) is done.
+  static constexpr int kSlots = (D == 64) ? 11 : 5;
   static constexpr int kBoxBytes = 128 * 128;      // 128 rows x 64 bf16 columns
   static constexpr int kNumBox = D / 64;
   static constexpr int kTileBytes = kNumBox * kBoxBytes;
-  static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+  static constexpr int kSmemBytes = (2 + kSlots) * kTileBytes + 1024;
   static constexpr int kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kIdescQK = make_idesc_bf16_f32(128, 128, false);
@@ -113,13 +116,14 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                           // [2][tile]
-  uint8_t* sK = smem + 2 * Cfg::kTileBytes;                     // [stages][tile]
-  uint8_t* sV = sK + Cfg::kStages * Cfg::kTileBytes;            // [stages][tile]
+  uint8_t* sKV = smem + 2 * Cfg::kTileBytes;                    // [slots][tile]
 
   __shared__ uint64_t q_full;
-  __shared__ uint64_t k_full[Cfg::kStages], k_empty[Cfg::kStages];
-  __shared__ uint64_t v_full[Cfg::kStages], v_empty[Cfg::kStages];
-  __shared__ uint64_t s_full[2], p_full[2], o_done[2];
+  __shared__ uint64_t kv_full[Cfg::kSlots];
+  // s_full0: S_0(j) done.  iter_done[j % 4]: the last MMA of key block j done (S_1(j) when
+  // tile 1 is active), which also releases K(j) and V(j-1): the tensor pipe completes one
+  // thread's MMAs in issue order, so a commit covers everything issued before it.
+  __shared__ uint64_t s_full0, iter_done[kIterRing], p_full[2], o_done[2];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_holder;
   __shared__ int abort_flag;
@@ -131,14 +135,10 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
-    for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
+    for (int s = 0; s < Cfg::kSlots; ++s) mbar_init(&kv_full[s], 1);
+    for (int r = 0; r < kIterRing; ++r) mbar_init(&iter_done[r], 1);
+    mbar_init(&s_full0, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(&s_full[q], 1);
       mbar_init(&p_full[q], 128);
       mbar_init(&o_done[q], 1);
     }
@@ -171,32 +171,30 @@ __global__ void __launch_bounds__(320, 1)
                       u.b * p.Hq + u.head[q]);
       }
       const int zkv = u.b * p.Hkv + u.kvh;
+      const int n_items = 2 * n_iter;
       int issued = 0;
-      for (int j = 0; j < n_iter; ++j) {
-        const int s = j % Cfg::kStages;
-        const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
-        if (!mbar_wait(&k_empty[s], ph ^ 1u, abort_p, kPrefillWaitTimeoutNs)) break;
-        mbar_arrive_expect_tx(&k_full[s], Cfg::kTileBytes);
-        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-          tma_load_3d(sK + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmK, &k_full[s], kb * 64, j * 128, zkv);
-        if (!mbar_wait(&v_empty[s], ph ^ 1u, abort_p, kPrefillWaitTimeoutNs)) {
-          issued = j + 1;  // K of tile j is in flight, V is not
-          break;
+      for (int i = 0; i < n_items; ++i) {
+        const int s = i % Cfg::kSlots;
+        if (i >= Cfg::kSlots) {
+          // the slot held item e = i - kSlots: K(e/2) is free after key block e/2, V(e/2) after e/2 + 1
+          const int r = (i - Cfg::kSlots + 1) >> 1;
+          if (!mbar_wait(&iter_done[r % kIterRing], static_cast<uint32_t>(r / kIterRing) & 1u, abort_p,
+                         kPrefillWaitTimeoutNs))
+            break;
         }
-        mbar_arrive_expect_tx(&v_full[s], Cfg::kTileBytes);
+        mbar_arrive_expect_tx(&kv_full[s], Cfg::kTileBytes);
+        const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
         for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-          tma_load_3d(sV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmV, &v_full[s], kb * 64, j * 128, zkv);
-        issued = j + 1;
+          tma_load_3d(sKV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, &kv_full[s], kb * 64, (i >> 1) * 128,
+                      zkv);
+        issued = i + 1;
       }
       if (*abort_p) {
         // Let the copies still in flight land before the CTA exits.
         mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
-        for (int j = max(0, issued - Cfg::kStages); j < issued; ++j) {
-          const int s = j % Cfg::kStages;
-          const uint32_t ph = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
-          mbar_wait(&k_full[s], ph, abort_p, kPrefillWaitTimeoutNs);
-          mbar_wait(&v_full[s], ph, abort_p, kPrefillWaitTimeoutNs);
-        }
+        for (int i = max(0, issued - Cfg::kSlots); i < issued; ++i)
+          mbar_wait(&kv_full[i % Cfg::kSlots], static_cast<uint32_t>(i / Cfg::kSlots) & 1u, abort_p,
+                    kPrefillWaitTimeoutNs);
       }
     }
     __syncwarp();
@@ -207,22 +205,21 @@ __global__ void __launch_bounds__(320, 1)
     // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
     // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
     if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
       bool ok = mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
-      tc_fence_after();
       bool any_mma = false;
       for (int j = 0; ok && j <= n_iter; ++j) {
         const bool do_s = j < n_iter;  // S(j) = Q K(j)^T
         const bool do_pv = j > 0;      // O += P(j-1) V(j-1)
-        const int sk = j % Cfg::kStages;
-        const uint32_t phk = static_cast<uint32_t>(j / Cfg::kStages) & 1u;
-        const int sv = (j - 1 + Cfg::kStages) % Cfg::kStages;
-        const uint32_t phv = static_cast<uint32_t>((j - 1) / Cfg::kStages) & 1u;
-        bool k_ready = false;
-        if (do_pv) {
-          if (!(ok = mbar_wait(&v_full[sv], phv, abort_p, kPrefillWaitTimeoutNs))) break;
-          tc_fence_after();
-        }
+        const int sk = (2 * j) % Cfg::kSlots;  // K(j)
+        const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
+        // Waits for the copies sit right after a commit, where they cost the least.
+        if (do_pv && !(ok = mbar_wait(&kv_full[sv], static_cast<uint32_t>((2 * j - 1) / Cfg::kSlots) & 1u, abort_p,
+                                      kPrefillWaitTimeoutNs)))
+          break;
+        if (do_s && !(ok = mbar_wait(&kv_full[sk], static_cast<uint32_t>((2 * j) / Cfg::kSlots) & 1u, abort_p,
+                                     kPrefillWaitTimeoutNs)))
+          break;
         for (int q = 0; q < 2; ++q) {
           const int nkv_q = q ? u.nkv[1] : u.nkv[0];
           if (do_pv && j - 1 < nkv_q) {
@@ -233,37 +230,26 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t a_p = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
-              const uint64_t db = make_sdesc_sw128(sVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
+              const uint64_t db = make_sdesc_sw128(sKVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
               umma_ts(d_o, a_p + kk * 8, db, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
             }
-            umma_commit(&o_done[q]);
+            if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
           }
           if (do_s && j < nkv_q) {
-            if (!k_ready) {
-              if (!(ok = mbar_wait(&k_full[sk], phk, abort_p, kPrefillWaitTimeoutNs))) break;
-              tc_fence_after();
-              k_ready = true;
-            }
             const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
               const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
-              const uint64_t db = make_sdesc_sw128(sKa + sk * Cfg::kTileBytes + off, 16, 1024);
+              const uint64_t db = make_sdesc_sw128(sKVa + sk * Cfg::kTileBytes + off, 16, 1024);
               umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
             }
             any_mma = true;
-            umma_commit(&s_full[q]);
+            if (q == 0) umma_commit(&s_full0);
           }
         }
         if (!ok) break;
-        if (do_s) {
-          if (!k_ready) {  // neither tile needed K(j): still consume the stage in order
-            if (!(ok = mbar_wait(&k_full[sk], phk, abort_p, kPrefillWaitTimeoutNs))) break;
-          }
-          umma_commit(&k_empty[sk]);
-        }
-        if (do_pv) umma_commit(&v_empty[sv]);
+        umma_commit(&iter_done[j % kIterRing]);
       }
       if (any_mma) {  // every MMA has finished before TMEM is released
         umma_commit(&mma_drain);
@@ -289,7 +275,14 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
-      if (!(ok = mbar_wait(&s_full[q], static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
+      // S_q(j) ready: tile 0 on s_full0, tile 1 on the per-iteration barrier that follows S_1(j)
+      if (q == 0) {
+        if (!(ok = mbar_wait(&s_full0, static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
+      } else {
+        if (!(ok = mbar_wait(&iter_done[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
+                             kPrefillWaitTimeoutNs)))
+          break;
+      }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(t_s, sr);
@@ -344,11 +337,9 @@ __global__ void __launch_bounds__(320, 1)
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       l_run = l_run * corr + ((a01.x + a01.y) + (a23.x + a23.y));
       if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
-        // O holds the sum up to block j-1 relative to the old base: wait for that PV, rescale in TMEM
-        // (done after P is written so the registers of S are free).
-        if (!(ok = mbar_wait(&o_done[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
-          break;
-        tc_fence_after();
+        // O holds the sum up to block j-1 relative to the old base; PV_q(j-1) was issued before
+        // S_q(j), so it has completed by now. Rescale in TMEM (after P is written, so the
+        // registers of S are free).
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
@@ -365,7 +356,7 @@ __global__ void __launch_bounds__(320, 1)
     }
 
     if (ok && nkv > 0) {
-      ok = mbar_wait(&o_done[q], static_cast<uint32_t>(nkv - 1) & 1u, abort_p, kPrefillWaitTimeoutNs);
+      ok = mbar_wait(&o_done[q], 0, abort_p, kPrefillWaitTimeoutNs);
       tc_fence_after();
       if (ok) {
         const float inv_l = 1.f / l_run;
