@@ -33,7 +33,7 @@ namespace gb300 {
 
 constexpr uint64_t kPrefillWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;                   // log2 of the allowed growth of p
-constexpr int kIterRing = 4;                                // per-iteration completion barriers in flight
+constexpr int kIterRing = 8;  // per-key-block barriers in flight (kv_ready, iter_done)
 
 template <int D>
 struct PrefillCfg {
@@ -50,6 +50,10 @@ struct PrefillCfg {
   static constexpr int kThreads = 320;
   static constexpr uint32_t kIdescQK = make_idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, D, true);
+  // The producer runs up to about kSlots / 2 key blocks ahead of the MMA thread; the
+  // per-block barrier rings must be deeper than that, or a barrier would be re-armed for
+  // block j + kIterRing before block j's phase was consumed.
+  static_assert(kIterRing >= (kSlots + 1) / 2 + 2, "per-block barrier ring too shallow for the K/V ring");
 };
 
 struct PrefillParams {
@@ -119,8 +123,10 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sKV = smem + 2 * Cfg::kTileBytes;                    // [slots][tile]
 
   __shared__ uint64_t q_full;
-  __shared__ uint64_t kv_full[Cfg::kSlots];
-  // s_full0: S_0(j) done.  iter_done[j % 4]: the last MMA of key block j done (S_1(j) when
+  // kv_ready[j % kIterRing]: the data of key block j is in shared memory: K(j) (j < n_iter) and
+  // V(j-1) (j > 0) both complete on it, so the MMA thread waits once per block.
+  __shared__ uint64_t kv_ready[kIterRing];
+  // s_full0: S_0(j) done.  iter_done[j % kIterRing]: the last MMA of key block j done (S_1(j) when
   // tile 1 is active), which also releases K(j) and V(j-1): the tensor pipe completes one
   // thread's MMAs in issue order, so a commit covers everything issued before it.
   __shared__ uint64_t s_full0, iter_done[kIterRing], p_full[2], o_done[2];
@@ -135,7 +141,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
-    for (int s = 0; s < Cfg::kSlots; ++s) mbar_init(&kv_full[s], 1);
+    for (int r = 0; r < kIterRing; ++r) mbar_init(&kv_ready[r], 1);
     for (int r = 0; r < kIterRing; ++r) mbar_init(&iter_done[r], 1);
     mbar_init(&s_full0, 1);
     for (int q = 0; q < 2; ++q) {
@@ -172,7 +178,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       const int zkv = u.b * p.Hkv + u.kvh;
       const int n_items = 2 * n_iter;
-      int issued = 0;
       for (int i = 0; i < n_items; ++i) {
         const int s = i % Cfg::kSlots;
         if (i >= Cfg::kSlots) {
@@ -182,19 +187,23 @@ __global__ void __launch_bounds__(320, 1)
                          kPrefillWaitTimeoutNs))
             break;
         }
-        mbar_arrive_expect_tx(&kv_full[s], Cfg::kTileBytes);
+        // item i belongs to key block it = (i + 1) / 2 of the MMA loop: K(j) to block j, V(j) to block j + 1
+        const int it = (i + 1) >> 1;
+        uint64_t* rb = &kv_ready[it % kIterRing];
+        if (i == 0 || (i & 1)) {  // first item of block `it`: arm the barrier with the bytes of both tiles
+          const int ntiles = (it >= 1 ? 1 : 0) + (it < n_iter ? 1 : 0);
+          mbar_arrive_expect_tx(rb, ntiles * Cfg::kTileBytes);
+        }
         const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
         for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-          tma_load_3d(sKV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, &kv_full[s], kb * 64, (i >> 1) * 128,
-                      zkv);
-        issued = i + 1;
+          tma_load_3d(sKV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, rb, kb * 64, (i >> 1) * 128, zkv);
       }
       if (*abort_p) {
-        // Let the copies still in flight land before the CTA exits.
-        mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
-        for (int i = max(0, issued - Cfg::kSlots); i < issued; ++i)
-          mbar_wait(&kv_full[i % Cfg::kSlots], static_cast<uint32_t>(i / Cfg::kSlots) & 1u, abort_p,
-                    kPrefillWaitTimeoutNs);
+        // Give the copies still in flight time to land before the CTA exits (a few microseconds
+        // suffice; wait 1 ms of wall time).
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
       }
     }
     __syncwarp();
@@ -211,19 +220,24 @@ __global__ void __launch_bounds__(320, 1)
       for (int j = 0; ok && j <= n_iter; ++j) {
         const bool do_s = j < n_iter;  // S(j) = Q K(j)^T
         const bool do_pv = j > 0;      // O += P(j-1) V(j-1)
-        const int sk = (2 * j) % Cfg::kSlots;  // K(j)
+        const int sk = (2 * j) % Cfg::kSlots;      // K(j)
         const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
-        // Waits for the copies sit right after a commit, where they cost the least.
-        if (do_pv && !(ok = mbar_wait(&kv_full[sv], static_cast<uint32_t>((2 * j - 1) / Cfg::kSlots) & 1u, abort_p,
-                                      kPrefillWaitTimeoutNs)))
-          break;
-        if (do_s && !(ok = mbar_wait(&kv_full[sk], static_cast<uint32_t>((2 * j) / Cfg::kSlots) & 1u, abort_p,
-                                     kPrefillWaitTimeoutNs)))
+        // Test the block's data and the first P together right after the previous commit:
+        // the two shared-memory round trips overlap; wait only for what is not ready yet.
+        uint64_t* rb = &kv_ready[j % kIterRing];
+        const uint32_t rph = static_cast<uint32_t>(j / kIterRing) & 1u;
+        const bool need_p0 = do_pv && j - 1 < u.nkv[0];
+        const bool data_ok = mbar_try_wait(rb, rph);
+        const bool p0_ok = need_p0 ? mbar_try_wait(&p_full[0], static_cast<uint32_t>(j - 1) & 1u) : true;
+        if (!data_ok && !(ok = mbar_wait(rb, rph, abort_p, kPrefillWaitTimeoutNs))) break;
+        if (!p0_ok && !(ok = mbar_wait(&p_full[0], static_cast<uint32_t>(j - 1) & 1u, abort_p,
+                                       kPrefillWaitTimeoutNs)))
           break;
         for (int q = 0; q < 2; ++q) {
           const int nkv_q = q ? u.nkv[1] : u.nkv[0];
           if (do_pv && j - 1 < nkv_q) {
-            if (!(ok = mbar_wait(&p_full[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
+            if (q == 1 &&
+                !(ok = mbar_wait(&p_full[1], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
               break;
             tc_fence_after();
             const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
@@ -294,19 +308,18 @@ __global__ void __launch_bounds__(320, 1)
         for (int k = 0; k < 128; ++k)
           if (j0 + k > lim) sr[k] = __float_as_uint(-INFINITY);
       }
-      // row max over columns 0..127: 4 pairwise seeds, then 15 rounds of 3-input max
-      float mx0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
-      float mx1 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
-      float mx2 = fmaxf(__uint_as_float(sr[4]), __uint_as_float(sr[5]));
-      float mx3 = fmaxf(__uint_as_float(sr[6]), __uint_as_float(sr[7]));
+      // row max over columns 0..127: 8 independent chains (pairwise seeds, then 7 rounds of
+      // 3-input max), merged at the end
+      float mx[8];
 #pragma unroll
-      for (int k = 8; k < 128; k += 8) {
-        mx0 = fmax3(mx0, __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
-        mx2 = fmax3(mx2, __uint_as_float(sr[k + 4]), __uint_as_float(sr[k + 5]));
-        mx3 = fmax3(mx3, __uint_as_float(sr[k + 6]), __uint_as_float(sr[k + 7]));
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+#pragma unroll
+      for (int k = 16; k < 128; k += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(sr[k + 2 * i]), __uint_as_float(sr[k + 2 * i + 1]));
       }
-      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_blk = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
       const float m_cand = fmaxf(m_run, m_blk);
       const bool grow = m_cand > m_run + kRescaleThreshold;
       float corr = 1.f;
