@@ -10,12 +10,16 @@
 // as the online softmax ("Module 07: Fused operators and FlashAttention",
 // section "Online softmax: derivation", the Step).
 //
-// Kernel 1 (split): one CTA per (split, KV head, sequence). One producer
-// thread streams the split's K and V rows into a ring of shared-memory stages
-// with bulk asynchronous copies (each stage = TILE contiguous rows, completing
-// on an mbarrier); four consumer warps read the stages with 16-byte shared
-// loads, keep a running (m, l, o) per query head of the group in registers,
-// merge them at the end and write one fp32 partial per (sequence, head, split).
+// Kernel 1 (split): one CTA per (split, K/V head, block of <= 4 query heads of
+// its group, sequence). One producer thread streams the split's K and V rows
+// into a ring of shared-memory stages with bulk asynchronous copies (each stage
+// = 32 contiguous rows, completing on an mbarrier); four consumer warps read
+// the stages with 16-byte shared loads (d/8 lanes per row, packed fp32x2 FMAs,
+// a shuffle reduction per head), keep a running (m, l, o) per query
+// head in registers, merge them at the end and write one fp32 partial per
+// (sequence, head, split). The exponent base only moves when a block maximum
+// exceeds it by more than 2^8, as in the prefill kernel: the normalised result
+// does not depend on the base.
 // Kernel 2 (combine): one CTA per (sequence, query head) merges the partials
 // of the non-empty splits in split order and writes O (bf16) and LSE.
 //
@@ -28,13 +32,17 @@
 namespace gb300 {
 
 constexpr uint64_t kDecodeWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr float kDecodeRescaleThreshold = 8.0f;           // log2 of the allowed growth of p
+constexpr int kDecodeMaxHeadsPerCta = 4;                  // query heads one CTA keeps in registers
 
 template <int D>
 struct DecodeCfg {
-  static constexpr int kLanesPerTok = D / 8;          // 16-byte slice per lane
+  static constexpr int kLanesPerTok = D / 8;           // one 16-byte chunk (8 elements) per lane
+  static constexpr int kChunks = 1;                    // 16-byte chunks per lane per row
+  static constexpr int kElems = 8 * kChunks;           // row elements per lane
   static constexpr int kTokPerPass = 32 / kLanesPerTok;
   static constexpr int kConsumerWarps = 4;
-  static constexpr int kTile = 32;                    // rows (tokens) per stage
+  static constexpr int kTile = 32;                     // rows (tokens) per stage
   static constexpr int kStages = 4;
   static constexpr int kTokPerWarp = kTile / kConsumerWarps;
   static constexpr int kPasses = kTokPerWarp / kTokPerPass;
@@ -51,13 +59,33 @@ struct DecodeParams {
   float* o_part;   // [B, Hq, S, D]
   float* ml_part;  // [B, Hq, S, 2]
   int Hq, Hkv, g, Lcap, S, C;
+  int n_hblk;      // CTAs per K/V head (query heads of a group split in blocks of <= 4)
+  int hblk;        // query heads per CTA
   float c;         // scale * log2(e)
 };
+
+// Lane layout inside a consumer warp: lane = grp * (D/8) + sub. The D/8 lanes of group
+// grp share one key row per pass; lane sub holds the 16-byte chunk sub of the row, so
+// every 8-lane phase of a 16-byte shared load touches 128 contiguous bytes.
+template <int D>
+__device__ __forceinline__ void load_row_chunks(const uint8_t* row, int sub, float (&f)[DecodeCfg<D>::kElems]) {
+#pragma unroll
+  for (int ch = 0; ch < DecodeCfg<D>::kChunks; ++ch) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + (sub + 8 * ch) * 16);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[ch * 8 + 2 * e] = bf16lo_to_f32(u[e]);
+      f[ch * 8 + 2 * e + 1] = bf16hi_to_f32(u[e]);
+    }
+  }
+}
 
 template <int D, int G>
 __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     decode_split_kernel(const DecodeParams p) {
   using Cfg = DecodeCfg<D>;
+  constexpr int E = Cfg::kElems;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;                                       // [stages][tile][D] bf16
@@ -67,8 +95,11 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   __shared__ int abort_flag;
 
   const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
+  const int kvh = blockIdx.y / p.n_hblk;
+  const int hb = blockIdx.y % p.n_hblk;
   const int b = blockIdx.z;
+  const int h0 = kvh * p.g + hb * p.hblk;                   // first query head of this CTA
+  const int nh = min(p.hblk, (kvh + 1) * p.g - h0);         // heads of this CTA (<= G)
   int L = p.seqlens[b];
   L = L < 0 ? 0 : (L > p.Lcap ? p.Lcap : L);
   const int start = split * p.C;
@@ -96,6 +127,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   if (warp == Cfg::kConsumerWarps) {
     // ---------------- producer: one thread issues the bulk copies ----------------
     if (lane == 0) {
+      int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % Cfg::kStages;
         const uint32_t ph = static_cast<uint32_t>(t / Cfg::kStages) & 1u;
@@ -106,9 +138,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
         bulk_copy_g2s(sK + s * Cfg::kTileBytes, kbase + static_cast<size_t>(row0) * D, bytes, &full_bar[s]);
         bulk_copy_g2s(sV + s * Cfg::kTileBytes, vbase + static_cast<size_t>(row0) * D, bytes, &full_bar[s]);
+        issued = t + 1;
       }
       // Let every copy this thread issued land before the CTA can exit.
-      for (int t = max(0, ntiles - Cfg::kStages); t < ntiles; ++t) {
+      for (int t = max(0, issued - Cfg::kStages); t < issued; ++t) {
         const int s = t % Cfg::kStages;
         mbar_wait(&full_bar[s], static_cast<uint32_t>(t / Cfg::kStages) & 1u, abort_p, kDecodeWaitTimeoutNs);
       }
@@ -119,28 +152,32 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   }
 
   // ---------------- consumers ----------------
-  const int grp = lane / Cfg::kLanesPerTok;   // which token of a pass
-  const int sub = lane % Cfg::kLanesPerTok;   // which 8-element slice of the row
+  const int grp = lane / Cfg::kLanesPerTok;  // which row of a pass
+  const int sub = lane % Cfg::kLanesPerTok;  // which chunk of the row
 
-  float qf[G][8];
+  float qf[G][E];
 #pragma unroll
   for (int gh = 0; gh < G; ++gh) {
-    const int h = kvh * p.g + gh;
-    const uint4 qv = *reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.Hq + h) * D + sub * 8);
-    const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
+    const bool have = gh < nh;
+    const __nv_bfloat16* qrow = p.q + (static_cast<size_t>(b) * p.Hq + (have ? h0 + gh : h0)) * D;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qf[gh][2 * e] = bf16lo_to_f32(u[e]) * p.c;
-      qf[gh][2 * e + 1] = bf16hi_to_f32(u[e]) * p.c;
+    for (int ch = 0; ch < Cfg::kChunks; ++ch) {
+      const uint4 qv = *reinterpret_cast<const uint4*>(qrow + (sub + 8 * ch) * 8);
+      const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qf[gh][ch * 8 + 2 * e] = have ? bf16lo_to_f32(u[e]) * p.c : 0.f;
+        qf[gh][ch * 8 + 2 * e + 1] = have ? bf16hi_to_f32(u[e]) * p.c : 0.f;
+      }
     }
   }
-  float m[G], l[G], o[G][8];
+  float m[G], l[G], o[G][E];
 #pragma unroll
   for (int gh = 0; gh < G; ++gh) {
     m[gh] = -INFINITY;
     l[gh] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[gh][e] = 0.f;
+    for (int e = 0; e < E; ++e) o[gh][e] = 0.f;
   }
 
   for (int t = 0; t < ntiles; ++t) {
@@ -151,66 +188,80 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     const uint8_t* vt = sV + s * Cfg::kTileBytes;
     const int row0 = start + t * Cfg::kTile;
 
+    // scores of this lane group's rows: s = (c q) . k, packed fp32x2 FMAs, shuffle reduction
     float sc[Cfg::kPasses][G];
 #pragma unroll
     for (int u = 0; u < Cfg::kPasses; ++u) {
       const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
       const bool valid = row0 + tok < end;
-      float kf[8];
-      const uint4 kv = valid ? *reinterpret_cast<const uint4*>(kt + tok * D * 2 + sub * 16) : make_uint4(0, 0, 0, 0);
-      const uint32_t ku[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16lo_to_f32(ku[e]);
-        kf[2 * e + 1] = bf16hi_to_f32(ku[e]);
-      }
+      float kf[E];
+      load_row_chunks<D>(kt + tok * D * 2, sub, kf);  // rows past `end` hold stale data: masked below
 #pragma unroll
       for (int gh = 0; gh < G; ++gh) {
-        float part = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) part = fmaf(qf[gh][e], kf[e], part);
+        for (int e = 0; e < E; e += 2)
+          acc = __ffma2_rn(make_float2(qf[gh][e], qf[gh][e + 1]), make_float2(kf[e], kf[e + 1]), acc);
+        float part = acc.x + acc.y;
 #pragma unroll
         for (int off = Cfg::kLanesPerTok / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
         sc[u][gh] = valid ? part : -INFINITY;
       }
     }
-    // block update of the running (m, l, o) of this lane group, per head
+    // running (m, l) update per head; the base only moves when the block max grows by > 2^8
     float pw[Cfg::kPasses][G];
+    bool grow_any = false;
+    float corr[G];
 #pragma unroll
     for (int gh = 0; gh < G; ++gh) {
       float mt = sc[0][gh];
 #pragma unroll
       for (int u = 1; u < Cfg::kPasses; ++u) mt = fmaxf(mt, sc[u][gh]);
-      const float mn = fmaxf(m[gh], mt);
-      const float base = (mn == -INFINITY) ? 0.f : mn;
-      const float corr = ex2_approx(m[gh] - base);
+      const float m_cand = fmaxf(m[gh], mt);
+      const bool grow = m_cand > m[gh] + kDecodeRescaleThreshold;
+      corr[gh] = 1.f;
+      if (grow) {
+        corr[gh] = ex2_approx(m[gh] - m_cand);  // 0 when m was -inf
+        m[gh] = m_cand;
+      }
+      grow_any |= grow;
+      const float base = (m[gh] == -INFINITY) ? 0.f : m[gh];
       float sum = 0.f;
 #pragma unroll
       for (int u = 0; u < Cfg::kPasses; ++u) {
         pw[u][gh] = ex2_approx(sc[u][gh] - base);
         sum += pw[u][gh];
       }
-      l[gh] = l[gh] * corr + sum;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[gh][e] *= corr;
-      m[gh] = mn;
+      l[gh] = l[gh] * corr[gh] + sum;
     }
+    if (__any_sync(0xFFFFFFFFu, grow_any)) {
+#pragma unroll
+      for (int gh = 0; gh < G; ++gh) {
+        const float2 c2 = make_float2(corr[gh], corr[gh]);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 r = __fmul2_rn(make_float2(o[gh][e], o[gh][e + 1]), c2);
+          o[gh][e] = r.x;
+          o[gh][e + 1] = r.y;
+        }
+      }
+    }
+    // o += p v over this lane group's rows
 #pragma unroll
     for (int u = 0; u < Cfg::kPasses; ++u) {
       const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
       if (row0 + tok < end) {
-        const uint4 vv = *reinterpret_cast<const uint4*>(vt + tok * D * 2 + sub * 16);
-        const uint32_t vu[4] = {vv.x, vv.y, vv.z, vv.w};
-        float vf[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          vf[2 * e] = bf16lo_to_f32(vu[e]);
-          vf[2 * e + 1] = bf16hi_to_f32(vu[e]);
-        }
+        float vf[E];
+        load_row_chunks<D>(vt + tok * D * 2, sub, vf);
 #pragma unroll
         for (int gh = 0; gh < G; ++gh) {
+          const float2 p2 = make_float2(pw[u][gh], pw[u][gh]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[gh][e] = fmaf(pw[u][gh], vf[e], o[gh][e]);
+          for (int e = 0; e < E; e += 2) {
+            const float2 r = __ffma2_rn(p2, make_float2(vf[e], vf[e + 1]), make_float2(o[gh][e], o[gh][e + 1]));
+            o[gh][e] = r.x;
+            o[gh][e + 1] = r.y;
+          }
         }
       }
     }
@@ -219,7 +270,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   }
   __syncwarp();
 
-  // merge the lane groups of this warp (same slice `sub`, different tokens)
+  // merge the lane groups of this warp (same chunks `sub`, different rows)
 #pragma unroll
   for (int off = Cfg::kLanesPerTok; off < 32; off <<= 1) {
 #pragma unroll
@@ -232,7 +283,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       const float w2 = ex2_approx(m2 - base);
       l[gh] = l[gh] * w1 + l2 * w2;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < E; ++e) {
         const float o2 = __shfl_xor_sync(0xFFFFFFFFu, o[gh][e], off);
         o[gh][e] = o[gh][e] * w1 + o2 * w2;
       }
@@ -249,7 +300,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     for (int gh = 0; gh < G; ++gh) {
       float* r = red + (warp * G + gh) * kRow;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r[sub * 8 + e] = o[gh][e];
+      for (int ch = 0; ch < Cfg::kChunks; ++ch)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[(sub + 8 * ch) * 8 + e] = o[gh][ch * 8 + e];
       if (sub == 0) {
         r[D] = m[gh];
         r[D + 1] = l[gh];
@@ -257,7 +310,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     }
   }
   named_bar_sync(1, 32 * Cfg::kConsumerWarps);
-  for (int idx = threadIdx.x; idx < G * D; idx += 32 * Cfg::kConsumerWarps) {
+  for (int idx = threadIdx.x; idx < nh * D; idx += 32 * Cfg::kConsumerWarps) {
     const int gh = idx / D;
     const int e = idx % D;
     float M = -INFINITY;
@@ -272,8 +325,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       acc += wt * r[e];
       lsum += wt * r[D + 1];
     }
-    const int h = kvh * p.g + gh;
-    const size_t slot = (static_cast<size_t>(b) * p.Hq + h) * p.S + split;
+    const size_t slot = (static_cast<size_t>(b) * p.Hq + h0 + gh) * p.S + split;
     p.o_part[slot * D + e] = acc;
     if (e == 0) {
       p.ml_part[slot * 2] = M;
@@ -283,12 +335,19 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   __syncthreads();
 }
 
+// One CTA per (sequence, query head): the weights 2^(m_s - M) of the non-empty splits
+// are computed once in shared memory, then every thread (one output element) sums its
+// column of partials in split order, so the result is deterministic for a given split count.
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ o_part,
                                                           const float* __restrict__ ml_part,
                                                           const int* __restrict__ seqlens,
                                                           __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                           int Hq, int S, int C, int Lcap) {
+  constexpr int kMaxSplitsInSmem = 1024;
+  __shared__ float w_s[kMaxSplitsInSmem];
+  __shared__ float red[D / 32];
+  __shared__ float Ms, Ls;
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   int L = seqlens[b];
@@ -297,19 +356,60 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
   const int e = threadIdx.x;
   const float* ml = ml_part + static_cast<size_t>(bh) * S * 2;
   const float* op = o_part + static_cast<size_t>(bh) * S * D;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+  // M = max_s m_s (block reduction)
+  float mloc = -INFINITY;
+  for (int s = e; s < nsplit; s += D) mloc = fmaxf(mloc, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, off));
+  if ((e & 31) == 0) red[e >> 5] = mloc;
+  __syncthreads();
+  if (e == 0) {
+    float M = -INFINITY;
+    for (int w = 0; w < D / 32; ++w) M = fmaxf(M, red[w]);
+    Ms = M;
+  }
+  __syncthreads();
+  const float M = Ms;
   if (nsplit == 0 || M == -INFINITY) {
     o[static_cast<size_t>(bh) * D + e] = __float2bfloat16_rn(0.f);
     if (e == 0 && lse != nullptr) lse[bh] = -INFINITY;
     return;
   }
-  float lsum = 0.f, acc = 0.f;
-  for (int s = 0; s < nsplit; ++s) {  // fixed split order: deterministic
+  const bool in_smem = nsplit <= kMaxSplitsInSmem;
+  // weights and the weighted sum of l: thread e takes splits e, e + D, ... (fixed order),
+  // then a fixed-shape block reduction, so the result does not depend on timing
+  float lpart = 0.f;
+  for (int s = e; s < nsplit; s += D) {
     const float w = ex2_approx(ml[2 * s] - M);
-    lsum = fmaf(w, ml[2 * s + 1], lsum);
-    acc = fmaf(w, op[static_cast<size_t>(s) * D + e], acc);
+    if (in_smem) w_s[s] = w;
+    lpart = fmaf(w, ml[2 * s + 1], lpart);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xFFFFFFFFu, lpart, off);
+  __syncthreads();  // red[] reuse and w_s complete
+  if ((e & 31) == 0) red[e >> 5] = lpart;
+  __syncthreads();
+  if (e == 0) {
+    float lsum = 0.f;
+    for (int w = 0; w < D / 32; ++w) lsum += red[w];
+    Ls = lsum;
+  }
+  float acc = 0.f;
+  int s = 0;
+  if (in_smem) {
+    for (; s + 4 <= nsplit; s += 4) {  // fixed order, four independent loads in flight
+      const float a0 = op[static_cast<size_t>(s) * D + e], a1 = op[static_cast<size_t>(s + 1) * D + e];
+      const float a2 = op[static_cast<size_t>(s + 2) * D + e], a3 = op[static_cast<size_t>(s + 3) * D + e];
+      acc = fmaf(w_s[s], a0, acc);
+      acc = fmaf(w_s[s + 1], a1, acc);
+      acc = fmaf(w_s[s + 2], a2, acc);
+      acc = fmaf(w_s[s + 3], a3, acc);
+    }
+  }
+  for (; s < nsplit; ++s)
+    acc = fmaf(in_smem ? w_s[s] : ex2_approx(ml[2 * s] - M), op[static_cast<size_t>(s) * D + e], acc);
+  __syncthreads();
+  const float lsum = Ls;
   o[static_cast<size_t>(bh) * D + e] = __float2bfloat16_rn(acc / lsum);
   if (e == 0 && lse != nullptr) lse[bh] = (M + log2f(lsum)) * 0.69314718055994530942f;
 }
@@ -320,22 +420,18 @@ static cudaError_t launch_split(const DecodeParams& p, int B, cudaStream_t strea
   auto kern = decode_split_kernel<D, G>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const dim3 grid(p.S, p.Hkv, B);
+  const dim3 grid(p.S, p.Hkv * p.n_hblk, B);
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int D>
 static cudaError_t launch_split_g(const DecodeParams& p, int B, cudaStream_t stream) {
-  switch (p.g) {
+  switch (p.hblk) {
     case 1: return launch_split<D, 1>(p, B, stream);
     case 2: return launch_split<D, 2>(p, B, stream);
     case 3: return launch_split<D, 3>(p, B, stream);
     case 4: return launch_split<D, 4>(p, B, stream);
-    case 5: return launch_split<D, 5>(p, B, stream);
-    case 6: return launch_split<D, 6>(p, B, stream);
-    case 7: return launch_split<D, 7>(p, B, stream);
-    case 8: return launch_split<D, 8>(p, B, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -355,10 +451,13 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
+  p.n_hblk = (p.g + kDecodeMaxHeadsPerCta - 1) / kDecodeMaxHeadsPerCta;
+  p.hblk = (p.g + p.n_hblk - 1) / p.n_hblk;
   p.Lcap = Lcap;
   p.S = S;
   p.C = C;
   p.c = scale * 1.4426950408889634f;
+  if (static_cast<long long>(Hkv) * p.n_hblk > 65535) return cudaErrorInvalidValue;
   cudaError_t err = (d == 64) ? launch_split_g<64>(p, B, stream) : launch_split_g<128>(p, B, stream);
   if (err != cudaSuccess) return err;
   *launched = 1;
