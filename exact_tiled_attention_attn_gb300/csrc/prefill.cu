@@ -12,10 +12,15 @@
 // How it maps onto the GPU (one CTA per work unit of two 128-row query tiles that
 // share one K/V stream: two query heads of the same K/V group at the same rows, or,
 // when the group size is odd, two consecutive row tiles of one head):
-//   warp 8      TMA producer: Q tiles once, then K and V tiles into 2-3 stage rings
+//   warp 8      TMA producer: Q tiles once, then K and V tiles into one ring of slots
 //               (128-byte swizzled boxes of 64 columns x 128 rows).
 //   warp 9      MMA issuer (one thread): S_q = Q_q K^T into TMEM (fp32), then
 //               O_q += P_q V with P read from TMEM (bf16) and V from shared memory.
+//   warp 10     waits for the issuer: it sits in the shared-memory barrier waits (the
+//               block's K/V, each tile's P) and hands each "go" to warp 9 through a
+//               hardware named barrier. One thread's tcgen05 queue holds about one MMA,
+//               so every wait the issuer did itself (~150+ clocks under load) would be
+//               tensor idle time; a named-barrier handoff costs tens of clocks.
 //   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1: one thread owns one
 //               row (TMEM lane), so row max and row sum need no shuffles; P is
 //               written back into the TMEM columns of S; O is rescaled in TMEM.
@@ -47,7 +52,7 @@ struct PrefillCfg {
   static constexpr int kTileBytes = kNumBox * kBoxBytes;
   static constexpr int kSmemBytes = (2 + kSlots) * kTileBytes + 1024;
   static constexpr int kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
   static constexpr uint32_t kIdescQK = make_idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescPV = make_idesc_bf16_f32(128, D, true);
   // The producer runs up to about kSlots / 2 key blocks ahead of the MMA thread; the
@@ -113,7 +118,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using Cfg = PrefillCfg<D>;
@@ -207,65 +212,79 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------ MMA issuer ------------------------------
-    // Issue order per key block j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The tensor pipe
-    // runs one thread's MMAs in issue order, so S_q(j) may overwrite the TMEM columns
-    // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
-    // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
-    if (lane == 0) {
-      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-      bool ok = mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
-      bool any_mma = false;
-      for (int j = 0; ok && j <= n_iter; ++j) {
-        const bool do_s = j < n_iter;  // S(j) = Q K(j)^T
-        const bool do_pv = j > 0;      // O += P(j-1) V(j-1)
-        const int sk = (2 * j) % Cfg::kSlots;      // K(j)
-        const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
-        // Test the block's data and the first P together right after the previous commit:
-        // the two shared-memory round trips overlap; wait only for what is not ready yet.
-        uint64_t* rb = &kv_ready[j % kIterRing];
-        const uint32_t rph = static_cast<uint32_t>(j / kIterRing) & 1u;
-        const bool need_p0 = do_pv && j - 1 < u.nkv[0];
-        const bool data_ok = mbar_try_wait(rb, rph);
-        const bool p0_ok = need_p0 ? mbar_try_wait(&p_full[0], static_cast<uint32_t>(j - 1) & 1u) : true;
-        if (!data_ok && !(ok = mbar_wait(rb, rph, abort_p, kPrefillWaitTimeoutNs))) break;
-        if (!p0_ok && !(ok = mbar_wait(&p_full[0], static_cast<uint32_t>(j - 1) & 1u, abort_p,
-                                       kPrefillWaitTimeoutNs)))
-          break;
+  } else if (warp == 9 || warp == 10) {
+    // Per key block j, tile q has work iff S_q(j) (j < nkv_q) or PV_q(j-1) (0 < j <= nkv_q).
+    // For each such (j, q) the helper (warp 10) arrives once on named barrier 1 + q after
+    // the waits, and the issuer (warp 9) syncs once on it before issuing: the two warps
+    // walk the same sequence, and an arrival for block j + 1 needs P_q(j), which needs
+    // S_q(j), which the issuer only issues after its sync for block j, so arrivals never
+    // run ahead of the matching sync. Arrivals are made even after an abort.
+    constexpr uint32_t kPair = 64;  // threads in each named-barrier rendezvous (two warps)
+    if (warp == 10) {
+      // ------------------------------ wait helper ------------------------------
+      if (lane == 0) mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
+      for (int j = 0; j <= n_iter; ++j) {
+        bool data_waited = false;
         for (int q = 0; q < 2; ++q) {
           const int nkv_q = q ? u.nkv[1] : u.nkv[0];
-          if (do_pv && j - 1 < nkv_q) {
-            if (q == 1 &&
-                !(ok = mbar_wait(&p_full[1], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs)))
-              break;
-            tc_fence_after();
-            const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
-            const uint32_t a_p = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
-#pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk) {
-              const uint64_t db = make_sdesc_sw128(sKVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
-              umma_ts(d_o, a_p + kk * 8, db, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
+          const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
+          if (!do_s && !do_pv) continue;
+          if (lane == 0 && !*abort_p) {
+            if (!data_waited)
+              mbar_wait(&kv_ready[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
+                        kPrefillWaitTimeoutNs);
+            if (do_pv) mbar_wait(&p_full[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs);
           }
-          if (do_s && j < nkv_q) {
+          data_waited = true;
+          __syncwarp();
+          named_bar_arrive(1 + q, kPair);
+        }
+      }
+    } else {
+      // ------------------------------ MMA issuer ------------------------------
+      // Issue order per key block j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The tensor pipe
+      // runs one thread's MMAs in issue order, so S_q(j) may overwrite the TMEM columns
+      // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
+      // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
+      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      bool any_mma = false;
+      for (int j = 0; j <= n_iter; ++j) {
+        const int sk = (2 * j) % Cfg::kSlots;      // K(j)
+        const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
+        for (int q = 0; q < 2; ++q) {
+          const int nkv_q = q ? u.nkv[1] : u.nkv[0];
+          const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
+          if (!do_s && !do_pv) continue;
+          __syncwarp();
+          named_bar_sync(1 + q, kPair);
+          if (lane == 0 && !*abort_p) {
+            tc_fence_after();
             const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+            if (do_pv) {
+              const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
-              const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
-              const uint64_t db = make_sdesc_sw128(sKVa + sk * Cfg::kTileBytes + off, 16, 1024);
-              umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 128 / 16; ++kk) {
+                const uint64_t db = make_sdesc_sw128(sKVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
+                umma_ts(d_o, d_s + kk * 8, db, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
+            }
+            if (do_s) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
+                const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
+                const uint64_t db = make_sdesc_sw128(sKVa + sk * Cfg::kTileBytes + off, 16, 1024);
+                umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+              }
+              if (q == 0) umma_commit(&s_full0);
             }
             any_mma = true;
-            if (q == 0) umma_commit(&s_full0);
           }
         }
-        if (!ok) break;
-        umma_commit(&iter_done[j % kIterRing]);
+        if (lane == 0) umma_commit(&iter_done[j % kIterRing]);
       }
-      if (any_mma) {  // every MMA has finished before TMEM is released
+      if (lane == 0 && any_mma) {  // every MMA has finished before TMEM is released
         umma_commit(&mma_drain);
         mbar_wait(&mma_drain, 0, abort_p, kPrefillWaitTimeoutNs);
       }
