@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(352, 1)
           if (!do_s && !do_pv) continue;
           __syncwarp();
           named_bar_sync(1 + q, kPair);
-          if (lane == 0 && !*abort_p) {
+          // No abort check here (a shared-memory load would stall the issue stream): after an
+          // abort the MMAs still only touch this CTA's buffers, and every waiter gives up.
+          if (lane == 0) {
             tc_fence_after();
             const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
             if (do_pv) {
