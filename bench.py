@@ -257,6 +257,30 @@ def run_gpu(args):
         e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
+    # ---- RMSNorm at growing T: the workload's 16.8 MB is launch- and latency-bound,
+    #      the sweep shows the kernel's sustained bandwidth (L2 flushed before each launch)
+    norm_sweep = []
+    if not args.no_e2e:
+        flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+        for Ts in (4096, 65536, 262144):
+            xs = torch.randn(Ts, NORM.D, device=dev).to(torch.bfloat16)
+            ys = torch.empty_like(xs)
+            tms = []
+            for _ in range(8):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                attn.rmsnorm(xs, wd, eps=NORM.eps, out=ys)
+                b.record(stream)
+                torch.cuda.synchronize()
+                tms.append(a.elapsed_time(b))
+            tms.sort()
+            bytes_s = 4 * Ts * NORM.D + 2 * NORM.D
+            norm_sweep.append({"T": Ts, "us": round(1e3 * tms[len(tms) // 2], 2),
+                               "GB/s": round(bytes_s / (tms[len(tms) // 2] * 1e-3) / 1e9, 1)})
+            del xs, ys
+        del flush
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_heads)
@@ -288,9 +312,11 @@ def run_gpu(args):
                          "flops_per_launch": flops},
             "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                        "frac": round(dec_gbs / peaks["hbm"], 4), "bytes_per_launch": dec_bytes,
-                       "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>"},
+                       "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>",
+                       "num_splits": splits},
             "rmsnorm": {"value": round(norm_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
-                        "frac": round(norm_gbs / peaks["hbm"], 4), "bytes_per_launch": norm_bytes},
+                        "frac": round(norm_gbs / peaks["hbm"], 4), "bytes_per_launch": norm_bytes,
+                        "sweep_D1024": norm_sweep},
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,
