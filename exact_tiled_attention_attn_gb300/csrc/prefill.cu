@@ -39,6 +39,10 @@ namespace gb300 {
 constexpr uint64_t kPrefillWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;                   // log2 of the allowed growth of p
 constexpr int kIterRing = 8;  // per-key-block barriers in flight (kv_ready, iter_done)
+// hardware named barriers (0 is __syncthreads) and their thread counts
+constexpr uint32_t kBarData = 1, kBarDataAck = 2, kBarP0 = 3;  // kBarP0 + 1 for tile 1
+constexpr uint32_t kPair = 64;                // helper warp + issuer warp
+constexpr uint32_t kSoftmaxAndIssuer = 160;   // 4 softmax warps + issuer warp
 
 template <int D>
 struct PrefillCfg {
@@ -117,6 +121,12 @@ __device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit
   return u;
 }
 
+// Key block j has MMA work iff some tile issues S_q(j) (j < nkv_q) or PV_q(j-1) (0 < j <= nkv_q).
+__device__ __forceinline__ bool block_has_work(const UnitInfo& u, int j) {
+  const int n = max(u.nkv[0], u.nkv[1]);
+  return j <= n && (j < n || j > 0);
+}
+
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -134,7 +144,7 @@ __global__ void __launch_bounds__(352, 1)
   // s_full0: S_0(j) done.  iter_done[j % kIterRing]: the last MMA of key block j done (S_1(j) when
   // tile 1 is active), which also releases K(j) and V(j-1): the tensor pipe completes one
   // thread's MMAs in issue order, so a commit covers everything issued before it.
-  __shared__ uint64_t s_full0, iter_done[kIterRing], p_full[2], o_done[2];
+  __shared__ uint64_t s_full0, iter_done[kIterRing], o_done[2];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_holder;
   __shared__ int abort_flag;
@@ -150,7 +160,6 @@ __global__ void __launch_bounds__(352, 1)
     for (int r = 0; r < kIterRing; ++r) mbar_init(&iter_done[r], 1);
     mbar_init(&s_full0, 1);
     for (int q = 0; q < 2; ++q) {
-      mbar_init(&p_full[q], 128);
       mbar_init(&o_done[q], 1);
     }
     mbar_init(&mma_drain, 1);
@@ -213,32 +222,28 @@ __global__ void __launch_bounds__(352, 1)
     }
     __syncwarp();
   } else if (warp == 9 || warp == 10) {
-    // Per key block j, tile q has work iff S_q(j) (j < nkv_q) or PV_q(j-1) (0 < j <= nkv_q).
-    // For each such (j, q) the helper (warp 10) arrives once on named barrier 1 + q after
-    // the waits, and the issuer (warp 9) syncs once on it before issuing: the two warps
-    // walk the same sequence, and an arrival for block j + 1 needs P_q(j), which needs
-    // S_q(j), which the issuer only issues after its sync for block j, so arrivals never
-    // run ahead of the matching sync. Arrivals are made even after an abort.
-    constexpr uint32_t kPair = 64;  // threads in each named-barrier rendezvous (two warps)
+    // Handoffs to the issuer go through hardware named barriers (bar.sync cannot time
+    // out, so every arrival sequence below runs to the end even after an abort, and each
+    // one matches the issuer's syncs one for one):
+    //  * data of key block j (when any tile has work in it): the helper arrives on kBarData,
+    //    the issuer syncs and acknowledges on kBarDataAck, the helper syncs on the ack;
+    //  * P_q(j) written: the 128 softmax threads of tile q arrive on kBarP0 + q and the
+    //    issuer syncs before PV_q(j). An arrival for P_q(j + 1) needs S_q(j + 1), which
+    //    the issuer only issues after its sync for P_q(j), so arrivals never run ahead.
     if (warp == 10) {
       // ------------------------------ wait helper ------------------------------
+      // Waits until block j's K/V data is in shared memory, then hands it to the issuer
+      // (kBarData) and waits for the issuer's acknowledgement (kBarDataAck) before looking
+      // at block j + 1, so the two warps stay in lockstep.
       if (lane == 0) mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
       for (int j = 0; j <= n_iter; ++j) {
-        bool data_waited = false;
-        for (int q = 0; q < 2; ++q) {
-          const int nkv_q = q ? u.nkv[1] : u.nkv[0];
-          const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
-          if (!do_s && !do_pv) continue;
-          if (lane == 0 && !*abort_p) {
-            if (!data_waited)
-              mbar_wait(&kv_ready[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
-                        kPrefillWaitTimeoutNs);
-            if (do_pv) mbar_wait(&p_full[q], static_cast<uint32_t>(j - 1) & 1u, abort_p, kPrefillWaitTimeoutNs);
-          }
-          data_waited = true;
-          __syncwarp();
-          named_bar_arrive(1 + q, kPair);
-        }
+        if (!block_has_work(u, j)) continue;
+        if (lane == 0 && !*abort_p)
+          mbar_wait(&kv_ready[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
+                    kPrefillWaitTimeoutNs);
+        __syncwarp();
+        named_bar_arrive(kBarData, kPair);
+        named_bar_sync(kBarDataAck, kPair);
       }
     } else {
       // ------------------------------ MMA issuer ------------------------------
@@ -251,12 +256,19 @@ __global__ void __launch_bounds__(352, 1)
       for (int j = 0; j <= n_iter; ++j) {
         const int sk = (2 * j) % Cfg::kSlots;      // K(j)
         const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
+        if (block_has_work(u, j)) {
+          __syncwarp();
+          named_bar_sync(kBarData, kPair);
+          named_bar_arrive(kBarDataAck, kPair);
+        }
         for (int q = 0; q < 2; ++q) {
           const int nkv_q = q ? u.nkv[1] : u.nkv[0];
           const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
           if (!do_s && !do_pv) continue;
-          __syncwarp();
-          named_bar_sync(1 + q, kPair);
+          if (do_pv) {
+            __syncwarp();
+            named_bar_sync(kBarP0 + q, kSoftmaxAndIssuer);
+          }
           // No abort check here (a shared-memory load would stall the issue stream): after an
           // abort the MMAs still only touch this CTA's buffers, and every waiter gives up.
           if (lane == 0) {
@@ -310,14 +322,16 @@ __global__ void __launch_bounds__(352, 1)
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
-      // S_q(j) ready: tile 0 on s_full0, tile 1 on the per-iteration barrier that follows S_1(j)
-      if (q == 0) {
-        if (!(ok = mbar_wait(&s_full0, static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs))) break;
-      } else {
-        if (!(ok = mbar_wait(&iter_done[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
-                             kPrefillWaitTimeoutNs)))
-          break;
+      // S_q(j) ready: tile 0 on s_full0, tile 1 on the per-iteration barrier that follows S_1(j).
+      // After a failed wait the warp skips the work but still arrives on the named barrier
+      // below, once per block, so the issuer's syncs always complete.
+      if (ok) {
+        const bool w = (q == 0) ? mbar_wait(&s_full0, static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs)
+                                : mbar_wait(&iter_done[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u,
+                                            abort_p, kPrefillWaitTimeoutNs);
+        ok = __all_sync(0xFFFFFFFFu, w);
       }
+      if (ok) {
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(t_s, sr);
@@ -383,10 +397,11 @@ __global__ void __launch_bounds__(352, 1)
           tmem_st32(t_o + cc * 32, ov);
         }
       }
+      }  // ok
 
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[q]);
+      named_bar_arrive(kBarP0 + q, kSoftmaxAndIssuer);  // P_q(j) (and any O rescale) is in TMEM
     }
 
     if (ok && nkv > 0) {

@@ -10,6 +10,9 @@ MMA thread and two softmax warpgroups with mbarriers:
 * iter_done[j % R]: committed after the last MMA of key block j; waited by the
   producer (slot reuse) and by softmax group 1 (S_1(j) ready).
 * s_full0 (S_0(j) ready) and p_full[q] (P_q(j) written), one phase per block.
+  In the kernel the P handoff (and the data handoff from a helper warp to the
+  MMA thread) are hardware named barriers that alternate strictly with the
+  issuer's syncs; the model keeps them as barriers with the same phase order.
 
 Waits use phase parity, so a ring of R barriers is only sound if no agent can
 get R phases ahead of another on the same barrier. This model runs the same
