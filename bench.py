@@ -125,6 +125,28 @@ def _dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of per-rank numbers over the default process group.
+
+    Every rank gets the maximum (the slowest rank sets the whole job's time). With
+    no process group, or a single rank, the values come back unchanged.
+    """
+    import torch
+    import torch.distributed as dist
+    vals = [float(v) for v in values]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return vals
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(a) for a in t.tolist()]
+
+
+def whole_job_rate(work_per_rank: float, ms_max: float, world: int) -> float:
+    """Units per second of the whole job: every rank did `work_per_rank` units, and the
+    job took as long as its slowest rank (`ms_max`)."""
+    return world * work_per_rank / (ms_max * 1e-3)
+
+
 def run_gpu(args):
     import torch
     import exact_tiled_attention_attn_gb300 as attn
@@ -209,10 +231,7 @@ def run_gpu(args):
     norm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    if world > 1:
-        t = torch.tensor([total_ms, fwd_ms, dec_ms, norm_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, fwd_ms, dec_ms, norm_ms = [float(a) for a in t.tolist()]
+    total_ms, fwd_ms, dec_ms, norm_ms = max_over_ranks([total_ms, fwd_ms, dec_ms, norm_ms], dev)
 
     peaks = _peaks()
     flops = PREFILL.flops()
@@ -223,7 +242,7 @@ def run_gpu(args):
     prefill_tflops = flops / (fwd_ms * 1e-3) / 1e12
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
     norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9
-    value = world * prefill_tflops
+    value = whole_job_rate(flops, fwd_ms, world) / 1e12
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -251,10 +270,10 @@ def run_gpu(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_ms = max_over_ranks([a.elapsed_time(b) / n_e2e], dev)[0]
         h2d = (q.numel() + k.numel() + v.numel()) * 2
         d2h = q.numel() * 2 + lsed.numel() * 4
-        e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e = {"value": round(whole_job_rate(flops, e2e_ms, world) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     # ---- RMSNorm at growing T: the workload's 16.8 MB is launch- and latency-bound,

@@ -16,14 +16,17 @@
 //               (128-byte swizzled boxes of 64 columns x 128 rows).
 //   warp 9      MMA issuer (one thread): S_q = Q_q K^T into TMEM (fp32), then
 //               O_q += P_q V with P read from TMEM (bf16) and V from shared memory.
-//   warp 10     waits for the issuer: it sits in the shared-memory barrier waits (the
-//               block's K/V, each tile's P) and hands each "go" to warp 9 through a
-//               hardware named barrier. One thread's tcgen05 queue holds about one MMA,
-//               so every wait the issuer did itself (~150+ clocks under load) would be
-//               tensor idle time; a named-barrier handoff costs tens of clocks.
+//   warp 10     waits for the issuer: it sits in the shared-memory barrier waits for
+//               Q and each key block's K/V and hands each "go" to warp 9 through a
+//               hardware named barrier (with an acknowledgement, so the two stay in
+//               step). One thread's tcgen05 queue holds about one MMA, so every wait
+//               the issuer did itself (~150+ clocks under load) would be tensor idle
+//               time; a named-barrier handoff costs tens of clocks.
 //   warps 0-3   softmax for query tile 0, warps 4-7 for tile 1: one thread owns one
 //               row (TMEM lane), so row max and row sum need no shuffles; P is
-//               written back into the TMEM columns of S; O is rescaled in TMEM.
+//               written back into the TMEM columns of S and its readiness goes to
+//               warp 9 through a named barrier shared by the tile's four warps and the
+//               issuer; O is rescaled in TMEM.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_q aliases the first 64 columns of S_q.
 //
@@ -251,18 +254,25 @@ __global__ void __launch_bounds__(352, 1)
       // runs one thread's MMAs in issue order, so S_q(j) may overwrite the TMEM columns
       // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
       // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
-      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      // Descriptors advance by adding (byte offset >> 4) to the start-address field: every
+      // operand lies in this CTA's shared memory window (< 256 KB), so no field overflows.
+      constexpr uint32_t kTile16 = Cfg::kTileBytes >> 4, kRing16 = Cfg::kSlots * kTile16;
+      const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = make_sdesc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dV = make_sdesc_sw128(smem_u32(sKV), Cfg::kBoxBytes, 1024);
+      const int nkv0 = u.nkv[0], nkv1 = u.nkv[1];
+      uint32_t k16 = 0;                  // slot of K(j), in 16-byte units
+      uint32_t v16 = kRing16 - kTile16;  // slot of V(j-1), used only when j > 0
       bool any_mma = false;
       for (int j = 0; j <= n_iter; ++j) {
-        const int sk = (2 * j) % Cfg::kSlots;      // K(j)
-        const int sv = (2 * j - 1) % Cfg::kSlots;  // V(j-1), used only when j > 0
         if (block_has_work(u, j)) {
           __syncwarp();
           named_bar_sync(kBarData, kPair);
           named_bar_arrive(kBarDataAck, kPair);
         }
+#pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const int nkv_q = q ? u.nkv[1] : u.nkv[0];
+          const int nkv_q = q ? nkv1 : nkv0;
           const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
           if (!do_s && !do_pv) continue;
           if (do_pv) {
@@ -277,19 +287,15 @@ __global__ void __launch_bounds__(352, 1)
             if (do_pv) {
               const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
 #pragma unroll
-              for (int kk = 0; kk < 128 / 16; ++kk) {
-                const uint64_t db = make_sdesc_sw128(sKVa + sv * Cfg::kTileBytes + kk * 2048, Cfg::kBoxBytes, 1024);
-                umma_ts(d_o, d_s + kk * 8, db, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < 128 / 16; ++kk)  // 16 keys = 2048 bytes of V per step
+                umma_ts(d_o, d_s + kk * 8, dV + v16 + kk * 128, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
               if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
             }
             if (do_s) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
-                const uint64_t da = make_sdesc_sw128(sQa + q * Cfg::kTileBytes + off, 16, 1024);
-                const uint64_t db = make_sdesc_sw128(sKVa + sk * Cfg::kTileBytes + off, 16, 1024);
-                umma_ss(d_s, da, db, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+                const uint32_t off16 = ((kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32) >> 4;
+                umma_ss(d_s, dQ + q * kTile16 + off16, dK + k16 + off16, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
               }
               if (q == 0) umma_commit(&s_full0);
             }
@@ -297,6 +303,10 @@ __global__ void __launch_bounds__(352, 1)
           }
         }
         if (lane == 0) umma_commit(&iter_done[j % kIterRing]);
+        v16 = k16 + kTile16;  // V(j) sits in the slot after K(j)
+        if (v16 >= kRing16) v16 -= kRing16;
+        k16 += 2 * kTile16;
+        if (k16 >= kRing16) k16 -= kRing16;
       }
       if (lane == 0 && any_mma) {  // every MMA has finished before TMEM is released
         umma_commit(&mma_drain);
