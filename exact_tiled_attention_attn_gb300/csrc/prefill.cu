@@ -75,6 +75,7 @@ struct PrefillParams {
   int causal;
   int pair_heads;  // 1: tiles are heads (2p, 2p+1) at the same rows; 0: row tiles (2p, 2p+1) of one head
   int n_qt;        // number of query tiles of 128 rows
+  int units;       // work units (pairs of query tiles), heaviest first when causal
   float c;         // scale * log2(e)
 };
 
@@ -130,6 +131,15 @@ __device__ __forceinline__ bool block_has_work(const UnitInfo& u, int j) {
   return j <= n && (j < n || j > 0);
 }
 
+// The CTAs are persistent: CTA c takes units in rounds of gridDim.x, in a snake order
+// (c in even rounds, gridDim.x - 1 - c in odd ones), so with the units sorted heaviest
+// first the CTAs' total work stays balanced without any shared counter.
+__device__ __forceinline__ int unit_index(int round) {
+  const int base = round * static_cast<int>(gridDim.x);
+  return (round & 1) ? base + static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                     : base + static_cast<int>(blockIdx.x);
+}
+
 template <int D>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -144,24 +154,23 @@ __global__ void __launch_bounds__(352, 1)
   // kv_ready[j % kIterRing]: the data of key block j is in shared memory: K(j) (j < n_iter) and
   // V(j-1) (j > 0) both complete on it, so the MMA thread waits once per block.
   __shared__ uint64_t kv_ready[kIterRing];
-  // s_full0: S_0(j) done.  iter_done[j % kIterRing]: the last MMA of key block j done (S_1(j) when
-  // tile 1 is active), which also releases K(j) and V(j-1): the tensor pipe completes one
-  // thread's MMAs in issue order, so a commit covers everything issued before it.
-  __shared__ uint64_t s_full0, iter_done[kIterRing], o_done[2];
+  // s_full1: S_1(j) done (one phase per S_1 block; tile 1 may be inactive in a unit).
+  // iter_done[j % kIterRing]: the last MMA of key block j done (S_0(j) when j < nkv_0), which
+  // also releases K(j) and V(j-1): the tensor pipe completes one thread's MMAs in issue
+  // order, so a commit covers everything issued before it.
+  __shared__ uint64_t s_full1, iter_done[kIterRing], o_done[2];
   __shared__ uint64_t mma_drain;
   __shared__ uint32_t tmem_base_holder;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const UnitInfo u = decode_unit(p, blockIdx.x);
-  const int n_iter = max(u.nkv[0], u.nkv[1]);
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
     for (int r = 0; r < kIterRing; ++r) mbar_init(&kv_ready[r], 1);
     for (int r = 0; r < kIterRing; ++r) mbar_init(&iter_done[r], 1);
-    mbar_init(&s_full0, 1);
+    mbar_init(&s_full1, 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(&o_done[q], 1);
     }
@@ -179,41 +188,74 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = tmem_base_holder;
   volatile int* abort_p = &abort_flag;
 
+  // Every role walks the same units in the same order and keeps the barrier phases running
+  // across them: G = index of the unit's key block 0 in this CTA's sequence of key blocks
+  // (a unit with n = max(nkv) has blocks 0..n, so G grows by n + 1 per unit).
   if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      const int nq = (u.nkv[0] > 0) + (u.nkv[1] > 0);
-      mbar_arrive_expect_tx(&q_full, nq * Cfg::kTileBytes);
-      for (int q = 0; q < 2; ++q) {
-        if (u.nkv[q] == 0) continue;
-        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-          tma_load_3d(sQ + q * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmQ, &q_full, kb * 64, u.row0[q],
-                      u.b * p.Hq + u.head[q]);
-      }
-      const int zkv = u.b * p.Hkv + u.kvh;
-      const int n_items = 2 * n_iter;
-      for (int i = 0; i < n_items; ++i) {
-        const int s = i % Cfg::kSlots;
-        if (i >= Cfg::kSlots) {
-          // the slot held item e = i - kSlots: K(e/2) is free after key block e/2, V(e/2) after e/2 + 1
-          const int r = (i - Cfg::kSlots + 1) >> 1;
-          if (!mbar_wait(&iter_done[r % kIterRing], static_cast<uint32_t>(r / kIterRing) & 1u, abort_p,
-                         kPrefillWaitTimeoutNs))
-            break;
+      int G = 0, U = 0;
+      int slot = 0;        // slot of the next item
+      int filled = 0;      // items loaded so far (saturates at kSlots)
+      int rel[Cfg::kSlots];  // block whose last MMA releases the item now in each slot
+      // Blocks complete in order (one thread issues all MMAs and commits), so a block at or
+      // below the last one seen complete needs no wait. Skipping those waits also keeps every
+      // wait less than kIterRing phases behind the ring: without it, a slot last used many
+      // one-block units ago would be waited on after its barrier had wrapped twice.
+      int done_upto = -1;
+      auto wait_block = [&](int r) -> bool {
+        if (r <= done_upto) return true;
+        if (!mbar_wait(&iter_done[r % kIterRing], static_cast<uint32_t>(r / kIterRing) & 1u, abort_p,
+                       kPrefillWaitTimeoutNs))
+          return false;
+        done_upto = r;
+        return true;
+      };
+      bool alive = true;
+      for (int round = 0; alive && round * static_cast<int>(gridDim.x) < p.units; ++round) {
+        const int idx = unit_index(round);
+        if (idx >= p.units) continue;
+        const UnitInfo u = decode_unit(p, idx);
+        const int n_iter = max(u.nkv[0], u.nkv[1]);
+        // this unit's Q overwrites the previous one's: wait for its last S MMAs (block G - 2)
+        if (U > 0 && !wait_block(G - 2)) break;
+        const int nq = (u.nkv[0] > 0) + (u.nkv[1] > 0);
+        mbar_arrive_expect_tx(&q_full, nq * Cfg::kTileBytes);
+        for (int q = 0; q < 2; ++q) {
+          if (u.nkv[q] == 0) continue;
+          for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+            tma_load_3d(sQ + q * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmQ, &q_full, kb * 64, u.row0[q],
+                        u.b * p.Hq + u.head[q]);
         }
-        // item i belongs to key block it = (i + 1) / 2 of the MMA loop: K(j) to block j, V(j) to block j + 1
-        const int it = (i + 1) >> 1;
-        uint64_t* rb = &kv_ready[it % kIterRing];
-        if (i == 0 || (i & 1)) {  // first item of block `it`: arm the barrier with the bytes of both tiles
-          const int ntiles = (it >= 1 ? 1 : 0) + (it < n_iter ? 1 : 0);
-          mbar_arrive_expect_tx(rb, ntiles * Cfg::kTileBytes);
+        const int zkv = u.b * p.Hkv + u.kvh;
+        const int n_items = 2 * n_iter;  // item 2j = K(j), item 2j + 1 = V(j)
+        for (int i = 0; i < n_items; ++i) {
+          if (filled == Cfg::kSlots) {
+            if (!wait_block(rel[slot])) {  // the slot's previous item is free once its block is done
+              alive = false;
+              break;
+            }
+          } else {
+            ++filled;
+          }
+          // item i belongs to key block it = (i + 1) / 2: K(j) is read in block j, V(j) in block j + 1
+          const int it = (i + 1) >> 1;
+          rel[slot] = G + it;
+          uint64_t* rb = &kv_ready[(G + it) % kIterRing];
+          if (i == 0 || (i & 1)) {  // first item of block `it`: arm the barrier with the bytes of both tiles
+            const int ntiles = (it >= 1 ? 1 : 0) + (it < n_iter ? 1 : 0);
+            mbar_arrive_expect_tx(rb, ntiles * Cfg::kTileBytes);
+          }
+          const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
+          for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+            tma_load_3d(sKV + slot * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, rb, kb * 64, (i >> 1) * 128, zkv);
+          if (++slot == Cfg::kSlots) slot = 0;
         }
-        const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
-        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-          tma_load_3d(sKV + s * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, rb, kb * 64, (i >> 1) * 128, zkv);
+        G += n_iter + 1;
+        ++U;
       }
       if (*abort_p) {
         // Give the copies still in flight time to land before the CTA exits (a few microseconds
@@ -235,78 +277,104 @@ __global__ void __launch_bounds__(352, 1)
     //    the issuer only issues after its sync for P_q(j), so arrivals never run ahead.
     if (warp == 10) {
       // ------------------------------ wait helper ------------------------------
-      // Waits until block j's K/V data is in shared memory, then hands it to the issuer
-      // (kBarData) and waits for the issuer's acknowledgement (kBarDataAck) before looking
-      // at block j + 1, so the two warps stay in lockstep.
-      if (lane == 0) mbar_wait(&q_full, 0, abort_p, kPrefillWaitTimeoutNs);
-      for (int j = 0; j <= n_iter; ++j) {
-        if (!block_has_work(u, j)) continue;
-        if (lane == 0 && !*abort_p)
-          mbar_wait(&kv_ready[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u, abort_p,
-                    kPrefillWaitTimeoutNs);
-        __syncwarp();
-        named_bar_arrive(kBarData, kPair);
-        named_bar_sync(kBarDataAck, kPair);
+      // Waits until the unit's Q and block j's K/V data are in shared memory, then hands
+      // them to the issuer (kBarData) and waits for the issuer's acknowledgement
+      // (kBarDataAck) before looking at block j + 1, so the two warps stay in lockstep.
+      int G = 0, U = 0;
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+        const int idx = unit_index(round);
+        if (idx >= p.units) continue;
+        const UnitInfo u = decode_unit(p, idx);
+        const int n_iter = max(u.nkv[0], u.nkv[1]);
+        if (lane == 0) mbar_wait(&q_full, static_cast<uint32_t>(U) & 1u, abort_p, kPrefillWaitTimeoutNs);
+        for (int j = 0; j <= n_iter; ++j) {
+          if (!block_has_work(u, j)) continue;
+          if (lane == 0 && !*abort_p)
+            mbar_wait(&kv_ready[(G + j) % kIterRing], static_cast<uint32_t>((G + j) / kIterRing) & 1u, abort_p,
+                      kPrefillWaitTimeoutNs);
+          __syncwarp();
+          named_bar_arrive(kBarData, kPair);
+          named_bar_sync(kBarDataAck, kPair);
+        }
+        G += n_iter + 1;
+        ++U;
       }
     } else {
       // ------------------------------ MMA issuer ------------------------------
-      // Issue order per key block j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The tensor pipe
+      // Issue order per key block j: PV_1(j-1), S_1(j), PV_0(j-1), S_0(j). The tensor pipe
       // runs one thread's MMAs in issue order, so S_q(j) may overwrite the TMEM columns
       // that PV_q(j-1) reads P_q(j-1) from, and softmax q gets S_q(j) two GEMMs after it
-      // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy.
+      // handed over P_q(j-1) while the other tile's GEMMs keep the tensor core busy. The
+      // next unit's PV_q(0) overwrites O_q only after the P_q(0) handoff, which the softmax
+      // warps of tile q give after they have read O_q for the previous unit.
+      // Tile 0 (active in every unit, nkv_0 >= max(nkv) - 1) learns of S_0(j) from the
+      // per-block ring, whose parity waits stay sound because its waits never skip more
+      // than a few blocks; tile 1, which may be inactive for a whole unit, has a barrier
+      // of its own with one phase per S_1 block.
       // Descriptors advance by adding (byte offset >> 4) to the start-address field: every
       // operand lies in this CTA's shared memory window (< 256 KB), so no field overflows.
       constexpr uint32_t kTile16 = Cfg::kTileBytes >> 4, kRing16 = Cfg::kSlots * kTile16;
       const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK = make_sdesc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dV = make_sdesc_sw128(smem_u32(sKV), Cfg::kBoxBytes, 1024);
-      const int nkv0 = u.nkv[0], nkv1 = u.nkv[1];
       uint32_t k16 = 0;                  // slot of K(j), in 16-byte units
       uint32_t v16 = kRing16 - kTile16;  // slot of V(j-1), used only when j > 0
       bool any_mma = false;
-      for (int j = 0; j <= n_iter; ++j) {
-        if (block_has_work(u, j)) {
-          __syncwarp();
-          named_bar_sync(kBarData, kPair);
-          named_bar_arrive(kBarDataAck, kPair);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int nkv_q = q ? nkv1 : nkv0;
-          const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
-          if (!do_s && !do_pv) continue;
-          if (do_pv) {
+      int G = 0;
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+        const int idx = unit_index(round);
+        if (idx >= p.units) continue;
+        const UnitInfo u = decode_unit(p, idx);
+        const int n_iter = max(u.nkv[0], u.nkv[1]);
+        const int nkv0 = u.nkv[0], nkv1 = u.nkv[1];
+        for (int j = 0; j <= n_iter; ++j) {
+          if (block_has_work(u, j)) {
             __syncwarp();
-            named_bar_sync(kBarP0 + q, kSoftmaxAndIssuer);
+            named_bar_sync(kBarData, kPair);
+            named_bar_arrive(kBarDataAck, kPair);
           }
-          // No abort check here (a shared-memory load would stall the issue stream): after an
-          // abort the MMAs still only touch this CTA's buffers, and every waiter gives up.
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const int q = 1 - qq;
+            const int nkv_q = q ? nkv1 : nkv0;
+            const bool do_s = j < nkv_q, do_pv = j > 0 && j - 1 < nkv_q;
+            if (!do_s && !do_pv) continue;
             if (do_pv) {
-              const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
-#pragma unroll
-              for (int kk = 0; kk < 128 / 16; ++kk)  // 16 keys = 2048 bytes of V per step
-                umma_ts(d_o, d_s + kk * 8, dV + v16 + kk * 128, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
-              if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
+              __syncwarp();
+              named_bar_sync(kBarP0 + q, kSoftmaxAndIssuer);
             }
-            if (do_s) {
+            // No abort check here (a shared-memory load would stall the issue stream): after an
+            // abort the MMAs still only touch this CTA's buffers, and every waiter gives up.
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t d_s = tmem + (q ? Cfg::kTmS1 : Cfg::kTmS0);
+              if (do_pv) {
+                const uint32_t d_o = tmem + (q ? Cfg::kTmO1 : Cfg::kTmO0);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off16 = ((kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32) >> 4;
-                umma_ss(d_s, dQ + q * kTile16 + off16, dK + k16 + off16, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 128 / 16; ++kk)  // 16 keys = 2048 bytes of V per step
+                  umma_ts(d_o, d_s + kk * 8, dV + v16 + kk * 128, Cfg::kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+                if (j == nkv_q) umma_commit(&o_done[q]);  // last block of this tile: O is final
               }
-              if (q == 0) umma_commit(&s_full0);
+              if (do_s) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off16 = ((kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32) >> 4;
+                  umma_ss(d_s, dQ + q * kTile16 + off16, dK + k16 + off16, Cfg::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                if (q == 1) umma_commit(&s_full1);
+              }
+              any_mma = true;
             }
-            any_mma = true;
+          }
+          if (lane == 0) umma_commit(&iter_done[(G + j) % kIterRing]);
+          if (j < n_iter) {  // the unit's 2 n_iter items: K(j) and V(j) for j < n_iter
+            v16 = k16 + kTile16;  // V(j) sits in the slot after K(j)
+            if (v16 >= kRing16) v16 -= kRing16;
+            k16 += 2 * kTile16;
+            if (k16 >= kRing16) k16 -= kRing16;
           }
         }
-        if (lane == 0) umma_commit(&iter_done[j % kIterRing]);
-        v16 = k16 + kTile16;  // V(j) sits in the slot after K(j)
-        if (v16 >= kRing16) v16 -= kRing16;
-        k16 += 2 * kTile16;
-        if (k16 >= kRing16) k16 -= kRing16;
+        G += n_iter + 1;
       }
       if (lane == 0 && any_mma) {  // every MMA has finished before TMEM is released
         umma_commit(&mma_drain);
@@ -318,27 +386,37 @@ __global__ void __launch_bounds__(352, 1)
     // ------------------------------ softmax warps ------------------------------
     const int q = warp >> 2;
     const int wq = warp & 3;
-    const int nkv = q ? u.nkv[1] : u.nkv[0];
-    const int row0 = q ? u.row0[1] : u.row0[0];
-    const int head = q ? u.head[1] : u.head[0];
     const int row_in_tile = wq * 32 + lane;
-    const int row = row0 + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + (q ? Cfg::kTmS1 : Cfg::kTmS0);
     const uint32_t t_o = tmem + lane_off + (q ? Cfg::kTmO1 : Cfg::kTmO0);
     const float c = p.c;
+    bool ok = true;
+    int G = 0;
+    int s1_count = 0;  // S_1 blocks committed in earlier units (phases of s_full1)
+    int o_count = 0;   // earlier units in which this tile was active (phases of o_done[q])
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+    const int idx = unit_index(round);
+    if (idx >= p.units) continue;
+    const UnitInfo u = decode_unit(p, idx);
+    const int n_iter = max(u.nkv[0], u.nkv[1]);
+    const int nkv = q ? u.nkv[1] : u.nkv[0];
+    const int row0 = q ? u.row0[1] : u.row0[0];
+    const int head = q ? u.head[1] : u.head[0];
+    const int row = row0 + row_in_tile;
     float m_run = -INFINITY;
     float l_run = 0.f;
-    bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
-      // S_q(j) ready: tile 0 on s_full0, tile 1 on the per-iteration barrier that follows S_1(j).
+      // S_q(j) ready: tile 1 on s_full1, tile 0 on the per-block barrier that follows S_0(j).
       // After a failed wait the warp skips the work but still arrives on the named barrier
       // below, once per block, so the issuer's syncs always complete.
       if (ok) {
-        const bool w = (q == 0) ? mbar_wait(&s_full0, static_cast<uint32_t>(j) & 1u, abort_p, kPrefillWaitTimeoutNs)
-                                : mbar_wait(&iter_done[j % kIterRing], static_cast<uint32_t>(j / kIterRing) & 1u,
-                                            abort_p, kPrefillWaitTimeoutNs);
+        const bool w = (q == 1) ? mbar_wait(&s_full1, static_cast<uint32_t>(s1_count + j) & 1u, abort_p,
+                                            kPrefillWaitTimeoutNs)
+                                : mbar_wait(&iter_done[(G + j) % kIterRing],
+                                            static_cast<uint32_t>((G + j) / kIterRing) & 1u, abort_p,
+                                            kPrefillWaitTimeoutNs);
         ok = __all_sync(0xFFFFFFFFu, w);
       }
       if (ok) {
@@ -415,7 +493,9 @@ __global__ void __launch_bounds__(352, 1)
     }
 
     if (ok && nkv > 0) {
-      ok = mbar_wait(&o_done[q], 0, abort_p, kPrefillWaitTimeoutNs);
+      // warp-uniform: the next unit's waits run under __all_sync
+      ok = __all_sync(0xFFFFFFFFu,
+                      mbar_wait(&o_done[q], static_cast<uint32_t>(o_count) & 1u, abort_p, kPrefillWaitTimeoutNs));
       tc_fence_after();
       if (ok) {
         const float inv_l = 1.f / l_run;
@@ -438,6 +518,10 @@ __global__ void __launch_bounds__(352, 1)
         if (store && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
       }
     }
+    s1_count += u.nkv[1];
+    o_count += (nkv > 0) ? 1 : 0;
+    G += n_iter + 1;
+    }  // units
     tc_fence_before();
   }
 
@@ -483,14 +567,35 @@ static bool make_map_3d(CUtensorMap* map, const void* base, int D, int rows, int
   return r == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (queried once per device).
+static int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) {
+    int n = 0;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : 0;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// One persistent CTA per SM (the shared memory allows one), or one per unit when there are fewer.
 template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                const PrefillParams& p, int units, cudaStream_t stream) {
+                                const PrefillParams& p, cudaStream_t stream) {
   using Cfg = PrefillCfg<D>;
   auto kern = attn_fwd_kernel<D>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<units, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, p);
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = p.units < sms ? p.units : sms;
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -516,9 +621,10 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   p.c = scale * 1.4426950408889634f;
   const long long units =
       p.pair_heads ? static_cast<long long>(p.n_qt) * (Hq / 2) * B : static_cast<long long>((p.n_qt + 1) / 2) * Hq * B;
-  if (units <= 0 || units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, static_cast<int>(units), stream)
-                 : launch_fwd_d<128>(mq, mk, mv, p, static_cast<int>(units), stream);
+  // (the kernel forms round * gridDim.x + gridDim.x in int)
+  if (units <= 0 || units > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+  p.units = static_cast<int>(units);
+  return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, stream) : launch_fwd_d<128>(mq, mk, mv, p, stream);
 }
 
 uint32_t prefill_take_device_error() { return take_device_error_word(); }

@@ -56,6 +56,17 @@ def test_prefill_grouping_modes(attn, d, causal, Hq, Hkv):
     assert_attn_close(o, lse, O, L, f"B2 Hq{Hq} Hkv{Hkv} d{d} causal{causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,T", [(16, 3, 3, 1100), (20, 4, 2, 640), (8, 5, 1, 1500)])
+def test_prefill_persistent_schedule(attn, d, causal, B, Hq, Hkv, T):
+    # More work units than SMs (240, 200, 240), so each persistent CTA walks several units of
+    # different lengths; with g odd and an odd tile count (9 tiles of 1100 rows) the last row
+    # pair of every head has an inactive second tile, first in the causal order, last otherwise.
+    o, lse, O, L = _prefill_case(attn, B, Hq, Hkv, T, T, d, causal, seed=700 + Hq + d + T)
+    assert_attn_close(o, lse, O, L, f"B{B} Hq{Hq} Hkv{Hkv} T{T} d{d} causal{causal}")
+
+
 @pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 255, 256, 257, 640])
 def test_prefill_lengths_and_tails(attn, T):
     for causal in (False, True):
