@@ -13,13 +13,14 @@ cites the passage of the source pages it writes out. The pages are:
 * "FlashAttention: attention without the n x n matrix" (GPU-internals lesson)
 * "Attention from the kernel's side: FlashAttention, online softmax and fused
   dequantisation" (note, in Polish)
-* "Chapter 5. Operators and runtime", section 5.3.3 "FlashAttention: tiling
-  and online softmax" (book chapter)
+* "Chapter 5. Operators and runtime", sections 5.3.3 "FlashAttention: tiling
+  and online softmax" and 5.4.3 (rounding and FP8 scales; book chapter)
+* "How does FlashAttention-3 work mathematically" (Q&A page), section 6 (FP8)
 
 Parity status: every function here is pinned by the tests in
-``tests/test_oracle_pins.py`` (worked examples printed on the pages, closed
-forms, brute force on tiny inputs, and the recurrence-equals-three-pass
-identity). No function is "parity unpinned".
+``tests/test_oracle_pins.py`` and ``tests/test_oracle_fp8_pins.py`` (worked
+examples printed on the pages, closed forms, brute force on tiny inputs, the
+recurrence-equals-three-pass identity, and the FP8 format's defining values). No function is "parity unpinned".
 """
 from .attention import (  # noqa: F401
     scores_softmax_weighted,
@@ -34,3 +35,14 @@ from .attention import (  # noqa: F401
     count_blocks,
 )
 from .rmsnorm import rmsnorm, rmsnorm_rows  # noqa: F401
+from .fp8 import (  # noqa: F401
+    E4M3_MAX,
+    e4m3_value,
+    e4m3_table,
+    e4m3_encode,
+    head_scale,
+    quantize_block,
+    quantize_kv,
+    dequantize_kv,
+    decode_fp8,
+)
