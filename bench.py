@@ -300,6 +300,36 @@ def run_gpu(args):
             del xs, ys
         del flush
 
+    # ---- FP8 (E4M3) KV-cache decode on the same workload (its own timing, outside the step):
+    #      the cache is quantised once on the GPU, then only the 1-byte codes are streamed
+    dec8 = None
+    if not args.no_fp8:
+        kq, ks = attn.kv_quantize_fp8(dkcd)
+        vq, vs = attn.kv_quantize_fp8(dvcd)
+        for _ in range(3):
+            attn.decode_fp8(dqd, kq, vq, ks, vs, dsld, scale=DECODE.scale, num_splits=splits, workspace=ws,
+                            out=dod, lse=dlse)
+        torch.cuda.synchronize()
+        n8 = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n8):
+            attn.decode_fp8(dqd, kq, vq, ks, vs, dsld, scale=DECODE.scale, num_splits=splits, workspace=ws,
+                            out=dod, lse=dlse)
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert attn.last_device_error() == 0
+        d8_ms = max_over_ranks([a.elapsed_time(b) / n8], dev)[0]
+        d8_bytes = (2 * DECODE.Hkv * DECODE.d * sum_l + 2 * DECODE.B * DECODE.Hq * DECODE.d * 2
+                    + DECODE.B * DECODE.Hq * 4 + DECODE.B * 4 + 2 * DECODE.B * DECODE.Hkv * 4)
+        d8_gbs = d8_bytes / (d8_ms * 1e-3) / 1e9
+        dec8 = {"value": round(d8_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
+                "frac": round(d8_gbs / peaks["hbm"], 4), "ms": round(d8_ms, 4), "bytes_per_launch": d8_bytes,
+                "vs_bf16_decode_time": round(dec_ms / d8_ms, 3),
+                "kernels": "decode_split_kernel<128,4,1> (E4M3 cache) + decode_combine_kernel<128>",
+                "num_splits": splits}
+        del kq, vq
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_heads)
@@ -336,6 +366,7 @@ def run_gpu(args):
             "rmsnorm": {"value": round(norm_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                         "frac": round(norm_gbs / peaks["hbm"], 4), "bytes_per_launch": norm_bytes,
                         "sweep_D1024": norm_sweep},
+            "decode_fp8": dec8,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,
@@ -461,6 +492,7 @@ def main():
                     help="DRAM bytes per prefill launch from an ncu capture, if known for this build")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV-cache decode line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -8,6 +8,8 @@ library's CUDA kernels. PyTorch provides device memory and streams.
     o, lse = fwd(q, k, v, causal=True)             # q [B,Hq,T,d], k/v [B,Hkv,T,d], bf16
     o, lse = decode(q, kcache, vcache, seqlens)     # q [B,Hq,d], caches [B,Hkv,Lcap,d]
     y = rmsnorm(x, w, eps=1e-6)                     # x [T,D], w [D]
+    codes, sc = kv_quantize_fp8(kcache)             # E4M3 codes (uint8) + fp32 scale per (b, head)
+    o, lse = decode_fp8(q, kcodes, vcodes, ksc, vsc, seqlens)
 """
 from __future__ import annotations
 
@@ -18,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "decode", "decode_noalloc", "rmsnorm", "decode_workspace_size", "default_splits",
+__all__ = ["fwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "decode_workspace_size",
+           "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
 
 
@@ -149,6 +152,66 @@ def decode_noalloc(q, kcache, vcache, seqlens, scale: float | None = None, num_s
                                          out.data_ptr(), lse.data_ptr() if lse is not None else None,
                                          B, Hq, Hkv, d, Lcap, float(scale), int(num_splits), _stream_ptr(stream))
     _lib.check("attn_decode_noalloc", st)
+    return out, lse
+
+
+def kv_quantize_fp8(x, codes=None, scale=None, stream=None):
+    """E4M3 codes of a bf16 cache x [B, H, L, d] with one fp32 scale per (b, h):
+    scale = amax / 448, code = RNE(x / scale) saturated at 448. Returns (codes uint8, scale)."""
+    _check_tensor("x", x, torch.bfloat16, 4)
+    B, H, L, d = x.shape
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    else:
+        _check_tensor("codes", codes, torch.uint8, 4)
+        if codes.shape != x.shape:
+            raise ValueError("codes must have the shape of x")
+    if scale is None:
+        scale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    else:
+        _check_tensor("scale", scale, torch.float32, 2)
+        if tuple(scale.shape) != (B, H):
+            raise ValueError("scale must be [B, H]")
+    st = _lib.load().attn_kv_quantize_fp8(x.data_ptr(), codes.data_ptr(), scale.data_ptr(), B, H, L, d,
+                                          _stream_ptr(stream))
+    _lib.check("attn_kv_quantize_fp8", st)
+    return codes, scale
+
+
+def decode_fp8(q, kcodes, vcodes, k_scale, v_scale, seqlens, scale: float | None = None,
+               num_splits: int | None = None, workspace=None, out=None, lse=None, return_lse: bool = True,
+               stream=None):
+    """Flash-decoding over an E4M3 KV cache (uint8 codes [B, Hkv, Lcap, d] and fp32
+    scales [B, Hkv], e.g. from kv_quantize_fp8), dequantised in registers."""
+    _check_tensor("q", q, torch.bfloat16, 3)
+    _check_tensor("kcodes", kcodes, torch.uint8, 4)
+    _check_tensor("vcodes", vcodes, torch.uint8, 4)
+    _check_tensor("k_scale", k_scale, torch.float32, 2)
+    _check_tensor("v_scale", v_scale, torch.float32, 2)
+    _check_tensor("seqlens", seqlens, torch.int32, 1)
+    B, Hq, d = q.shape
+    Hkv, Lcap = kcodes.shape[1], kcodes.shape[2]
+    if kcodes.shape != vcodes.shape or kcodes.shape[0] != B or kcodes.shape[3] != d:
+        raise ValueError("kcodes and vcodes must both be [B, Hkv, Lcap, d] matching q")
+    if tuple(k_scale.shape) != (B, Hkv) or tuple(v_scale.shape) != (B, Hkv):
+        raise ValueError("k_scale and v_scale must be [B, Hkv]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        num_splits = default_splits(B, Hkv, Lcap)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = _lib.load().attn_decode_fp8(q.data_ptr(), kcodes.data_ptr(), vcodes.data_ptr(), k_scale.data_ptr(),
+                                     v_scale.data_ptr(), seqlens.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr() if lse is not None else None, B, Hq, Hkv, d, Lcap, float(scale),
+                                     int(num_splits), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _lib.check("attn_decode_fp8", st)
     return out, lse
 
 

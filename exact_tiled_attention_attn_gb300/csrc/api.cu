@@ -10,9 +10,11 @@
 namespace gb300 {
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                             int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream);
-cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens, void* o, float* lse,
-                          int B, int Hq, int Hkv, int d, int Lcap, float scale, int S, int C, void* workspace,
-                          cudaStream_t stream, int* launched);
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const float* k_scale, const float* v_scale,
+                          const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap,
+                          float scale, int S, int C, void* workspace, cudaStream_t stream, int* launched);
+cudaError_t launch_kv_quantize_fp8(const void* x, void* codes, float* scale, int BH, long long per_head,
+                                   cudaStream_t stream, int* launched);
 cudaError_t launch_rmsnorm(const void* x, const void* w, void* y, int T, int D, float eps, cudaStream_t s);
 size_t decode_noalloc_capacity();
 cudaError_t decode_noalloc_scratch(void** ptr);
@@ -23,6 +25,26 @@ uint32_t rmsnorm_take_device_error();
 static std::atomic<unsigned long long> g_launches{0};
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by the decode entry points (everything but the workspace).
+static attn_status check_decode_args(const void* q, const void* kcache, const void* vcache, const int* seqlens,
+                                     const void* o, const float* lse, int B, int Hq, int Hkv, int d, int Lcap,
+                                     float scale, int num_splits) {
+  if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
+    return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
 
 static int decode_chunk(int Lcap, int num_splits) {
   const long long c = (static_cast<long long>(Lcap) + num_splits - 1) / num_splits;
@@ -88,26 +110,52 @@ int attn_decode_default_splits(int B, int Hkv, int Lcap) {
 attn_status attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
                         float* lse, int B, int Hq, int Hkv, int d, int Lcap, float scale, int num_splits,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
-    return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
-  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
-  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  const attn_status st =
+      check_decode_args(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits);
+  if (st != ATTN_OK) return st;
   if (workspace == nullptr || workspace_bytes < attn_decode_workspace_size(B, Hq, d, num_splits))
     return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
-  if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
-    return ATTN_ERR_UNSUPPORTED;
   const int C = decode_chunk(Lcap, num_splits);
   int launched = 0;
-  const cudaError_t err = launch_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits,
-                                        C, workspace, stream, &launched);
+  const cudaError_t err = launch_decode(q, kcache, vcache, nullptr, nullptr, seqlens, o, lse, B, Hq, Hkv, d, Lcap,
+                                        scale, num_splits, C, workspace, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_decode_fp8(const void* q, const void* kcache, const void* vcache, const float* k_scale,
+                            const float* v_scale, const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                            int d, int Lcap, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  const attn_status st =
+      check_decode_args(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits);
+  if (st != ATTN_OK) return st;
+  if (k_scale == nullptr || v_scale == nullptr) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < attn_decode_workspace_size(B, Hq, d, num_splits))
+    return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  const int C = decode_chunk(Lcap, num_splits);
+  int launched = 0;
+  const cudaError_t err = launch_decode(q, kcache, vcache, k_scale, v_scale, seqlens, o, lse, B, Hq, Hkv, d, Lcap,
+                                        scale, num_splits, C, workspace, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_kv_quantize_fp8(const void* x, void* codes, float* scale, int B, int H, int L, int d,
+                                 cudaStream_t stream) {
+  if (x == nullptr || codes == nullptr || scale == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || L < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (d % 8 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  int launched = 0;
+  const cudaError_t err = launch_kv_quantize_fp8(x, codes, scale, B * H, static_cast<long long>(L) * d, stream,
+                                                 &launched);
   g_launches.fetch_add(static_cast<unsigned long long>(launched));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -115,27 +163,17 @@ attn_status attn_decode(const void* q, const void* kcache, const void* vcache, c
 attn_status attn_decode_noalloc(const void* q, const void* kcache, const void* vcache, const int* seqlens,
                                 void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap, float scale,
                                 int num_splits, cudaStream_t stream) {
-  if (q == nullptr || kcache == nullptr || vcache == nullptr || seqlens == nullptr || o == nullptr)
-    return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
-  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return ATTN_ERR_MISALIGNED;
-  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
-  if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
-    return ATTN_ERR_UNSUPPORTED;
+  const attn_status st =
+      check_decode_args(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits);
+  if (st != ATTN_OK) return st;
   // The partials must fit the library's fixed scratch; refuse before touching the device.
   if (attn_decode_workspace_size(B, Hq, d, num_splits) > decode_noalloc_capacity()) return ATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (decode_noalloc_scratch(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
   const int C = decode_chunk(Lcap, num_splits);
   int launched = 0;
-  const cudaError_t err = launch_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, num_splits,
-                                        C, scratch, stream, &launched);
+  const cudaError_t err = launch_decode(q, kcache, vcache, nullptr, nullptr, seqlens, o, lse, B, Hq, Hkv, d, Lcap,
+                                        scale, num_splits, C, scratch, stream, &launched);
   g_launches.fetch_add(static_cast<unsigned long long>(launched));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

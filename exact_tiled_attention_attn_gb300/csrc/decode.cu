@@ -35,9 +35,10 @@ constexpr uint64_t kDecodeWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kDecodeRescaleThreshold = 8.0f;           // log2 of the allowed growth of p
 constexpr int kDecodeMaxHeadsPerCta = 4;                  // query heads one CTA keeps in registers
 
-template <int D>
+// EB = bytes per cached element: 2 for the bf16 cache, 1 for the E4M3 (FP8) cache.
+template <int D, int EB = 2>
 struct DecodeCfg {
-  static constexpr int kLanesPerTok = D / 8;           // one 16-byte chunk (8 elements) per lane
+  static constexpr int kLanesPerTok = D / 8;           // one chunk of 8 elements (8 * EB bytes) per lane
   static constexpr int kChunks = 1;                    // 16-byte chunks per lane per row
   static constexpr int kElems = 8 * kChunks;           // row elements per lane
   static constexpr int kTokPerPass = 32 / kLanesPerTok;
@@ -46,15 +47,18 @@ struct DecodeCfg {
   static constexpr int kStages = 4;
   static constexpr int kTokPerWarp = kTile / kConsumerWarps;
   static constexpr int kPasses = kTokPerWarp / kTokPerPass;
-  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kRowBytes = D * EB;
+  static constexpr int kTileBytes = kTile * kRowBytes;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);
   static constexpr int kSmemBytes = kStages * 2 * kTileBytes + 1024;
 };
 
 struct DecodeParams {
   const __nv_bfloat16* q;
-  const __nv_bfloat16* kc;
-  const __nv_bfloat16* vc;
+  const uint8_t* kc;       // [B, Hkv, Lcap, D] elements of EB bytes
+  const uint8_t* vc;
+  const float* k_scale;    // [B, Hkv] dequantisation scales of an E4M3 cache (nullptr for bf16)
+  const float* v_scale;
   const int* seqlens;
   float* o_part;   // [B, Hq, S, D]
   float* ml_part;  // [B, Hq, S, 2]
@@ -64,32 +68,56 @@ struct DecodeParams {
   float c;         // scale * log2(e)
 };
 
+// Two E4M3 codes (the low byte is the element at the lower address) -> two floats. The
+// conversion to f16 is exact (every E4M3 value is an f16 value), and so is f16 -> f32.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two_codes & 0xFFFFu)));
+  float lo, hi;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<unsigned short>(h2 >> 16)));
+  return make_float2(lo, hi);
+}
+
 // Lane layout inside a consumer warp: lane = grp * (D/8) + sub. The D/8 lanes of group
-// grp share one key row per pass; lane sub holds the 16-byte chunk sub of the row, so
-// every 8-lane phase of a 16-byte shared load touches 128 contiguous bytes.
-template <int D>
-__device__ __forceinline__ void load_row_chunks(const uint8_t* row, int sub, float (&f)[DecodeCfg<D>::kElems]) {
-#pragma unroll
-  for (int ch = 0; ch < DecodeCfg<D>::kChunks; ++ch) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + (sub + 8 * ch) * 16);
+// grp share one key row per pass; lane sub holds the elements 8 sub .. 8 sub + 7 of the
+// row (16 bytes of bf16 or 8 bytes of E4M3), so the lanes of a group read the row
+// contiguously.
+template <int D, int EB>
+__device__ __forceinline__ void load_row_chunks(const uint8_t* row, int sub, float (&f)[DecodeCfg<D, EB>::kElems]) {
+  static_assert(DecodeCfg<D, EB>::kChunks == 1, "one chunk of 8 elements per lane");
+  if constexpr (EB == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + sub * 16);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      f[ch * 8 + 2 * e] = bf16lo_to_f32(u[e]);
-      f[ch * 8 + 2 * e + 1] = bf16hi_to_f32(u[e]);
+      f[2 * e] = bf16lo_to_f32(u[e]);
+      f[2 * e + 1] = bf16hi_to_f32(u[e]);
+    }
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(row + sub * 8);
+    const uint32_t u[2] = {v.x, v.y};
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const float2 a = e4m3x2_to_float2(u[w]);
+      const float2 b = e4m3x2_to_float2(u[w] >> 16);
+      f[4 * w] = a.x;
+      f[4 * w + 1] = a.y;
+      f[4 * w + 2] = b.x;
+      f[4 * w + 3] = b.y;
     }
   }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
+template <int D, int G, int EB>
+__global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     decode_split_kernel(const DecodeParams p) {
-  using Cfg = DecodeCfg<D>;
+  using Cfg = DecodeCfg<D, EB>;
   constexpr int E = Cfg::kElems;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;                                       // [stages][tile][D] bf16
-  uint8_t* sV = smem + Cfg::kStages * Cfg::kTileBytes;      // [stages][tile][D] bf16
+  uint8_t* sK = smem;                                       // [stages][tile][D] elements
+  uint8_t* sV = smem + Cfg::kStages * Cfg::kTileBytes;      // [stages][tile][D] elements
   __shared__ uint64_t full_bar[Cfg::kStages];
   __shared__ uint64_t empty_bar[Cfg::kStages];
   __shared__ int abort_flag;
@@ -121,8 +149,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   volatile int* abort_p = &abort_flag;
 
   const size_t head_off = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Lcap;  // in rows
-  const __nv_bfloat16* kbase = p.kc + head_off * D;
-  const __nv_bfloat16* vbase = p.vc + head_off * D;
+  const uint8_t* kbase = p.kc + head_off * Cfg::kRowBytes;
+  const uint8_t* vbase = p.vc + head_off * Cfg::kRowBytes;
 
   if (warp == Cfg::kConsumerWarps) {
     // ---------------- producer: one thread issues the bulk copies ----------------
@@ -134,10 +162,10 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
         if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_p, kDecodeWaitTimeoutNs)) break;
         const int row0 = start + t * Cfg::kTile;
         const int nrows = min(Cfg::kTile, end - row0);
-        const uint32_t bytes = static_cast<uint32_t>(nrows) * D * 2;
+        const uint32_t bytes = static_cast<uint32_t>(nrows) * Cfg::kRowBytes;
         mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
-        bulk_copy_g2s(sK + s * Cfg::kTileBytes, kbase + static_cast<size_t>(row0) * D, bytes, &full_bar[s]);
-        bulk_copy_g2s(sV + s * Cfg::kTileBytes, vbase + static_cast<size_t>(row0) * D, bytes, &full_bar[s]);
+        bulk_copy_g2s(sK + s * Cfg::kTileBytes, kbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes, &full_bar[s]);
+        bulk_copy_g2s(sV + s * Cfg::kTileBytes, vbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes, &full_bar[s]);
         issued = t + 1;
       }
       // Let every copy this thread issued land before the CTA can exit.
@@ -155,6 +183,9 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
   const int grp = lane / Cfg::kLanesPerTok;  // which row of a pass
   const int sub = lane % Cfg::kLanesPerTok;  // which chunk of the row
 
+  // q is pre-multiplied by c = scale * log2(e) and, for an E4M3 cache, by the keys'
+  // dequantisation scale, so the scores come out of the raw codes' values directly
+  const float qmul = p.c * (p.k_scale != nullptr ? p.k_scale[static_cast<size_t>(b) * p.Hkv + kvh] : 1.f);
   float qf[G][E];
 #pragma unroll
   for (int gh = 0; gh < G; ++gh) {
@@ -166,8 +197,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       const uint32_t u[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        qf[gh][ch * 8 + 2 * e] = have ? bf16lo_to_f32(u[e]) * p.c : 0.f;
-        qf[gh][ch * 8 + 2 * e + 1] = have ? bf16hi_to_f32(u[e]) * p.c : 0.f;
+        qf[gh][ch * 8 + 2 * e] = have ? bf16lo_to_f32(u[e]) * qmul : 0.f;
+        qf[gh][ch * 8 + 2 * e + 1] = have ? bf16hi_to_f32(u[e]) * qmul : 0.f;
       }
     }
   }
@@ -195,7 +226,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
       const bool valid = row0 + tok < end;
       float kf[E];
-      load_row_chunks<D>(kt + tok * D * 2, sub, kf);  // rows past `end` hold stale data: masked below
+      load_row_chunks<D, EB>(kt + tok * Cfg::kRowBytes, sub, kf);  // rows past `end` hold stale data: masked below
 #pragma unroll
       for (int gh = 0; gh < G; ++gh) {
         float2 acc = make_float2(0.f, 0.f);
@@ -252,7 +283,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
       if (row0 + tok < end) {
         float vf[E];
-        load_row_chunks<D>(vt + tok * D * 2, sub, vf);
+        load_row_chunks<D, EB>(vt + tok * Cfg::kRowBytes, sub, vf);
 #pragma unroll
         for (int gh = 0; gh < G; ++gh) {
           const float2 p2 = make_float2(pw[u][gh], pw[u][gh]);
@@ -310,6 +341,8 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
     }
   }
   named_bar_sync(1, 32 * Cfg::kConsumerWarps);
+  // the values' dequantisation scale multiplies the weighted sum once, here
+  const float vmul = p.v_scale != nullptr ? p.v_scale[static_cast<size_t>(b) * p.Hkv + kvh] : 1.f;
   for (int idx = threadIdx.x; idx < nh * D; idx += 32 * Cfg::kConsumerWarps) {
     const int gh = idx / D;
     const int e = idx % D;
@@ -326,7 +359,7 @@ __global__ void __launch_bounds__(DecodeCfg<D>::kThreads)
       lsum += wt * r[D + 1];
     }
     const size_t slot = (static_cast<size_t>(b) * p.Hq + h0 + gh) * p.S + split;
-    p.o_part[slot * D + e] = acc;
+    p.o_part[slot * D + e] = acc * vmul;
     if (e == 0) {
       p.ml_part[slot * 2] = M;
       p.ml_part[slot * 2 + 1] = lsum;
@@ -414,10 +447,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
   if (e == 0 && lse != nullptr) lse[bh] = (M + log2f(lsum)) * 0.69314718055994530942f;
 }
 
-template <int D, int G>
+template <int D, int G, int EB>
 static cudaError_t launch_split(const DecodeParams& p, int B, cudaStream_t stream) {
-  using Cfg = DecodeCfg<D>;
-  auto kern = decode_split_kernel<D, G>;
+  using Cfg = DecodeCfg<D, EB>;
+  auto kern = decode_split_kernel<D, G, EB>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   const dim3 grid(p.S, p.Hkv * p.n_hblk, B);
@@ -425,26 +458,30 @@ static cudaError_t launch_split(const DecodeParams& p, int B, cudaStream_t strea
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, int EB>
 static cudaError_t launch_split_g(const DecodeParams& p, int B, cudaStream_t stream) {
   switch (p.hblk) {
-    case 1: return launch_split<D, 1>(p, B, stream);
-    case 2: return launch_split<D, 2>(p, B, stream);
-    case 3: return launch_split<D, 3>(p, B, stream);
-    case 4: return launch_split<D, 4>(p, B, stream);
+    case 1: return launch_split<D, 1, EB>(p, B, stream);
+    case 2: return launch_split<D, 2, EB>(p, B, stream);
+    case 3: return launch_split<D, 3, EB>(p, B, stream);
+    case 4: return launch_split<D, 4, EB>(p, B, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// Returns the number of kernels launched through *launched.
-cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int* seqlens, void* o, float* lse,
-                          int B, int Hq, int Hkv, int d, int Lcap, float scale, int S, int C, void* workspace,
-                          cudaStream_t stream, int* launched) {
+// Returns the number of kernels launched through *launched. k_scale/v_scale non-null
+// selects the E4M3 cache (one byte per element), else the cache is bf16.
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const float* k_scale, const float* v_scale,
+                          const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap,
+                          float scale, int S, int C, void* workspace, cudaStream_t stream, int* launched) {
   *launched = 0;
+  const bool fp8 = k_scale != nullptr;
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.kc = static_cast<const __nv_bfloat16*>(kc);
-  p.vc = static_cast<const __nv_bfloat16*>(vc);
+  p.kc = static_cast<const uint8_t*>(kc);
+  p.vc = static_cast<const uint8_t*>(vc);
+  p.k_scale = fp8 ? k_scale : nullptr;
+  p.v_scale = fp8 ? v_scale : nullptr;
   p.seqlens = seqlens;
   p.o_part = static_cast<float*>(workspace);
   p.ml_part = p.o_part + static_cast<size_t>(B) * Hq * S * d;
@@ -458,7 +495,8 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
   p.C = C;
   p.c = scale * 1.4426950408889634f;
   if (static_cast<long long>(Hkv) * p.n_hblk > 65535) return cudaErrorInvalidValue;
-  cudaError_t err = (d == 64) ? launch_split_g<64>(p, B, stream) : launch_split_g<128>(p, B, stream);
+  cudaError_t err = fp8 ? ((d == 64) ? launch_split_g<64, 1>(p, B, stream) : launch_split_g<128, 1>(p, B, stream))
+                        : ((d == 64) ? launch_split_g<64, 2>(p, B, stream) : launch_split_g<128, 2>(p, B, stream));
   if (err != cudaSuccess) return err;
   *launched = 1;
   if (d == 64) {

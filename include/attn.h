@@ -158,6 +158,52 @@ attn_status attn_decode_noalloc(const void* q, const void* kcache, const void* v
                                 int num_splits, cudaStream_t stream);
 
 /*
+ * attn_kv_quantize_fp8 - a bf16 KV cache written as E4M3 (FP8) codes with one
+ * scale per (sequence, head).
+ *
+ * Defined by: "Chapter 5. Operators and runtime", section 5.4.3, example 5-7
+ * (the E4M3 format: one sign, four exponent and three mantissa bits, largest
+ * finite value 448; a scale maps the largest magnitude of the block it covers
+ * onto 448, elements are divided by it and rounded to a representable value,
+ * code value x scale gives the element back) and "How does FlashAttention-3
+ * work mathematically", section 6 (E4M3 for K and V). The block a scale covers
+ * is the whole [L, d] slice of one (sequence, head).
+ *
+ *   x      bf16 [B, H, L, d], 16-byte aligned (device)
+ *   codes  uint8 [B, H, L, d] (written), 8-byte aligned: code = RNE(x / scale)
+ *          in E4M3, magnitudes above 448 saturated to 448
+ *   scale  fp32 [B, H] (written): amax / 448 as one correctly rounded fp32
+ *          division over the slice's largest magnitude; 1 for an all-zero slice
+ *   d a multiple of 8; B * H <= 65535. NaN inputs are outside the contract.
+ * Four kernel launches on `stream`; the result does not depend on their timing.
+ */
+attn_status attn_kv_quantize_fp8(const void* x, void* codes, float* scale, int B, int H, int L, int d,
+                                 cudaStream_t stream);
+
+/*
+ * attn_decode_fp8 - attn_decode over an E4M3 (FP8) KV cache, dequantised in
+ * registers as the tiles are read.
+ *
+ * Defined by: "Attention from the kernel's side: FlashAttention, online
+ * softmax and fused dequantisation", section "Why a quantised cache needs a
+ * fused kernel" (read the low-precision bytes straight into the kernel and
+ * turn them into values in registers: the traffic is the quantised cache and
+ * nothing more), with the format of attn_kv_quantize_fp8. The result is the
+ * attention of attn_decode over the dequantised keys and values
+ * code_value x scale.
+ *
+ *   kcache, vcache  uint8 E4M3 codes [B, Hkv, Lcap, d], 16-byte aligned
+ *   k_scale, v_scale  fp32 [B, Hkv] (device), the per-(sequence, head) scales
+ * Everything else (q, seqlens, o, lse, shapes, num_splits, the workspace and
+ * its size attn_decode_workspace_size, errors) as attn_decode.
+ */
+attn_status attn_decode_fp8(const void* q, const void* kcache, const void* vcache,
+                            const float* k_scale, const float* v_scale, const int* seqlens,
+                            void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap, float scale,
+                            int num_splits, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
  * rmsnorm_fwd - y = x / sqrt(mean_j x_j^2 + eps) * w for every row, one pass.
  *
  * Defined by: "Module 07: Fused operators and FlashAttention", section

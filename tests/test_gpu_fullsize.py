@@ -83,6 +83,27 @@ def test_decode_full_size(attn):
     assert_attn_close(o, lse, O, L, "decode full size")
 
 
+def test_decode_fp8_full_size(attn):
+    # the decode workload with its cache quantised to E4M3 on the GPU; the oracle quantises the
+    # sampled sequences itself (all their heads) and decodes them
+    shp = W.DECODE_LLAMA
+    q, kc, vc, sl = W.decode_inputs(shp)
+    kcodes, ksc = attn.kv_quantize_fp8(kc.to(DEV))
+    vcodes, vsc = attn.kv_quantize_fp8(vc.to(DEV))
+    S = attn.default_splits(shp.B, shp.Hkv, shp.Lcap)
+    o, lse = attn.decode_fp8(q.to(DEV), kcodes, vcodes, ksc, vsc, sl.to(DEV), num_splits=S)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    o, lse = f64(o), f64(lse)
+    for b in (0, shp.B - 1):
+        okc, oks = oracle.quantize_kv(f64(kc[b:b + 1]))
+        ovc, ovs = oracle.quantize_kv(f64(vc[b:b + 1]))
+        assert np.array_equal(ksc[b].cpu().numpy(), oks[0]) and np.array_equal(vsc[b].cpu().numpy(), ovs[0])
+        assert np.array_equal(kcodes[b, 0].cpu().numpy(), okc[0, 0])
+        Ob, Lb = oracle.decode_fp8(f64(q[b:b + 1]), okc, ovc, oks, ovs, sl[b:b + 1].numpy(), shp.scale)
+        assert_attn_close(o[b:b + 1], lse[b:b + 1], Ob, Lb, f"fp8 decode full size, sequence {b}")
+
+
 def test_rmsnorm_full_size(attn):
     x, w = W.norm_inputs(W.NORM_QWEN)
     y = attn.rmsnorm(x.to(DEV), w.to(DEV), eps=W.NORM_QWEN.eps)

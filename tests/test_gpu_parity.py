@@ -235,6 +235,82 @@ def test_decode_out_of_range_lengths_are_defined(attn):
     assert_attn_close(o[2:], lse[2:], O, L, "clamped length")
 
 
+# ----------------------------------------------------------------------------- FP8 (E4M3) KV cache
+
+def _assert_codes_equal(got, want, what):
+    got = got.cpu().numpy() if isinstance(got, torch.Tensor) else got
+    bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+    assert bad.size == 0, f"{what}: {bad.size} codes differ, first at {bad[:5]}: {got.reshape(-1)[bad[:5]]} vs " \
+                          f"{want.reshape(-1)[bad[:5]]}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_kv_quantize_fp8_matches_oracle_bytes(attn, d):
+    # heads of very different ranges: N(0,1), x 300 (codes near 448 after scaling), x 1e-3, an
+    # all-zero head (scale 1), a head with one large outlier (most codes subnormal)
+    gen = torch.Generator().manual_seed(900 + d)
+    x = torch.randn((2, 3, 300, d), generator=gen)
+    x[0, 1] *= 300.0
+    x[0, 2] *= 1e-3
+    x[1, 0] = 0.0
+    x[1, 1, 7, 3] = 5000.0
+    x = x.to(torch.bfloat16)
+    codes, sc = attn.kv_quantize_fp8(x.to(DEV))
+    torch.cuda.synchronize()
+    want_codes, want_sc = oracle.quantize_kv(f64(x))
+    assert np.array_equal(sc.cpu().numpy(), want_sc), (sc.cpu().numpy(), want_sc)
+    _assert_codes_equal(codes, want_codes, f"d{d}")
+
+
+def _decode_fp8_case(attn, B, Hq, Hkv, d, Lcap, lens, splits, seed):
+    shp = W.DecodeShape("t", B, Hq, Hkv, d, 1, Lcap, seed)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=lens)
+    kcodes, ksc = attn.kv_quantize_fp8(kc.to(DEV))
+    vcodes, vsc = attn.kv_quantize_fp8(vc.to(DEV))
+    okc, oks = oracle.quantize_kv(f64(kc))
+    ovc, ovs = oracle.quantize_kv(f64(vc))
+    O, L = oracle.decode_fp8(f64(q), okc, ovc, oks, ovs, sl.numpy(), shp.scale)
+    for S in splits:
+        o, lse = attn.decode_fp8(q.to(DEV), kcodes, vcodes, ksc, vsc, sl.to(DEV), num_splits=S)
+        torch.cuda.synchronize()
+        assert attn.last_device_error() == 0
+        assert_attn_close(o, lse, O, L, f"fp8 decode B{B} Hq{Hq} Hkv{Hkv} d{d} S{S}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 4), (8, 1), (6, 2)])
+def test_decode_fp8_groupings(attn, d, Hq, Hkv):
+    _decode_fp8_case(attn, 3, Hq, Hkv, d, 320, [1, 77, 320], [1, 4, 20], seed=950 + Hq + d)
+
+
+def test_decode_fp8_lengths_and_splits(attn):
+    lens = [1, 15, 16, 17, 33, 1000, 2048]
+    _decode_fp8_case(attn, len(lens), 8, 2, 128, 2048, lens, [1, 3, 64, 128], seed=970)
+
+
+def test_decode_fp8_equals_bf16_decode_on_lossless_cache(attn):
+    # a cache whose values are E4M3 values times 2^-6 with a 448 * 2^-6 maximum in every head
+    # quantises losslessly, so the FP8 path must agree with the bf16 path to the tolerance
+    gen = torch.Generator().manual_seed(980)
+    B, Hq, Hkv, d, L = 2, 8, 2, 128, 512
+    table = torch.tensor(oracle.e4m3_table()[:0x7F], dtype=torch.float32)
+    idx = torch.randint(0, 0x7F, (2, B, Hkv, L, d), generator=gen)
+    sign = torch.where(torch.rand((2, B, Hkv, L, d), generator=gen) < 0.5, -1.0, 1.0)
+    vals = table[idx] * sign * 2.0 ** -6
+    vals[:, :, :, 0, 0] = 448.0 * 2.0 ** -6
+    kc, vc = vals[0].to(torch.bfloat16), vals[1].to(torch.bfloat16)
+    assert torch.equal(kc.float(), vals[0]) and torch.equal(vc.float(), vals[1])
+    q = torch.randn((B, Hq, d), generator=gen).to(torch.bfloat16)
+    sl = torch.tensor([L, 300], dtype=torch.int32)
+    kcodes, ksc = attn.kv_quantize_fp8(kc.to(DEV))
+    vcodes, vsc = attn.kv_quantize_fp8(vc.to(DEV))
+    assert torch.all(ksc == 2.0 ** -6) and torch.all(vsc == 2.0 ** -6)
+    o8, l8 = attn.decode_fp8(q.to(DEV), kcodes, vcodes, ksc, vsc, sl.to(DEV), num_splits=4)
+    O, Lse = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), 1.0 / math.sqrt(d))
+    torch.cuda.synchronize()
+    assert_attn_close(o8, l8, O, Lse, "lossless fp8 cache")
+
+
 # ----------------------------------------------------------------------------- RMSNorm
 
 @pytest.mark.parametrize("T,D", [(1, 8), (37, 64), (300, 1000), (4096, 1024), (33, 4096), (5, 8192), (17, 2056)])
