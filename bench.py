@@ -42,6 +42,21 @@ DECODE = W.DECODE_LLAMA
 NORM = W.NORM_QWEN
 WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 
+# DRAM bytes (read + write) of one attn_fwd_kernel<128> launch on the prefill workload, from the
+# ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md,
+# with the SHA-256 of the kernel source it was taken with: the figure is reported only while
+# that source is unchanged.
+PREFILL_TRAFFIC = {"bytes": 343813120 + 95751680,
+                   "prefill_cu_sha256": "907c8818e7eeb9d0e26d4b72f8a47f26b8368c3870cd687790a9915494fe4116"}
+
+
+def prefill_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "exact_tiled_attention_attn_gb300", "csrc", "prefill.cu")
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return PREFILL_TRAFFIC["bytes"] if sha == PREFILL_TRAFFIC["prefill_cu_sha256"] else None
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -356,7 +371,10 @@ def run_gpu(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128>",
                          "achieved": round(prefill_tflops, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
-                         "frac": round(prefill_tflops / peaks["bf16"], 4), "traffic": args.traffic,
+                         "frac": round(prefill_tflops / peaks["bf16"], 4),
+                         "traffic": args.traffic if args.traffic is not None else prefill_traffic(),
+                         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                         "algorithmic_bytes": PREFILL.hbm_bytes(),
                          "peak_source": f"{peaks['source']} bf16 (burst)",
                          "flops_per_launch": flops},
             "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],

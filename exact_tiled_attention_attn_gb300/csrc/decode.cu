@@ -211,6 +211,23 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     for (int e = 0; e < E; ++e) o[gh][e] = 0.f;
   }
 
+  // Each lane group (LPR = D/8 lanes) takes R consecutive rows of the warp's share of a
+  // tile. Every lane computes its 8-element partial dot product for all R rows, then a
+  // transpose-reduce over the group (each shuffle step halves the rows a lane keeps)
+  // leaves the full score of row `my_row` in LPR/R lanes. The softmax runs once per row
+  // owner; l is accumulated per lane (duplicated over the LPR/R owners) and reduced at the
+  // end; p is broadcast back to the group for the P.V update, which every lane does for
+  // its 8 output elements.
+  constexpr int LPR = Cfg::kLanesPerTok;
+  constexpr int R = Cfg::kTokPerWarp / Cfg::kTokPerPass;   // rows per group per tile
+  constexpr int kRowLanes = LPR / R;                        // lanes holding one row's score
+  static_assert(R >= 1 && (R & (R - 1)) == 0 && kRowLanes >= 1, "rows per group must be a power of two");
+  int my_row = 0;  // row (0..R-1) whose score this lane ends up holding
+#pragma unroll
+  for (int off = LPR / 2, cnt = R / 2; cnt >= 1; off >>= 1, cnt >>= 1)
+    if (sub & off) my_row += cnt;
+  const int grp_lane0 = lane - sub;
+
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % Cfg::kStages;
     if (!mbar_wait(&full_bar[s], static_cast<uint32_t>(t / Cfg::kStages) & 1u, abort_p, kDecodeWaitTimeoutNs))
@@ -218,36 +235,56 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     const uint8_t* kt = sK + s * Cfg::kTileBytes;
     const uint8_t* vt = sV + s * Cfg::kTileBytes;
     const int row0 = start + t * Cfg::kTile;
+    const int tok0 = warp * Cfg::kTokPerWarp + grp * R;  // first row of this group in the tile
 
-    // scores of this lane group's rows: s = (c q) . k, packed fp32x2 FMAs, shuffle reduction
-    float sc[Cfg::kPasses][G];
+    // partial dot products of (c q) with this lane's 8 elements of each of the R rows
+    float part[R][G];
 #pragma unroll
-    for (int u = 0; u < Cfg::kPasses; ++u) {
-      const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
-      const bool valid = row0 + tok < end;
+    for (int u = 0; u < R; ++u) {
       float kf[E];
-      load_row_chunks<D, EB>(kt + tok * Cfg::kRowBytes, sub, kf);  // rows past `end` hold stale data: masked below
+      load_row_chunks<D, EB>(kt + (tok0 + u) * Cfg::kRowBytes, sub, kf);  // rows past `end`: masked below
 #pragma unroll
       for (int gh = 0; gh < G; ++gh) {
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < E; e += 2)
           acc = __ffma2_rn(make_float2(qf[gh][e], qf[gh][e + 1]), make_float2(kf[e], kf[e + 1]), acc);
-        float part = acc.x + acc.y;
-#pragma unroll
-        for (int off = Cfg::kLanesPerTok / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-        sc[u][gh] = valid ? part : -INFINITY;
+        part[u][gh] = acc.x + acc.y;
       }
     }
-    // running (m, l) update per head; the base only moves when the block max grows by > 2^8
-    float pw[Cfg::kPasses][G];
+    // transpose-reduce: at lane distance `off` the lanes with that bit set keep the upper
+    // half of their rows and receive their partner's partial sums for it
+#pragma unroll
+    for (int off = LPR / 2, cnt = R / 2; cnt >= 1; off >>= 1, cnt >>= 1) {
+      const bool upper = (sub & off) != 0;
+#pragma unroll
+      for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+        for (int gh = 0; gh < G; ++gh) {
+          const float keep = upper ? part[j + cnt][gh] : part[j][gh];
+          const float give = upper ? part[j][gh] : part[j + cnt][gh];
+          part[j][gh] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, off);
+        }
+      }
+    }
+    // the lanes that share a row finish its sum
+#pragma unroll
+    for (int off = kRowLanes / 2; off >= 1; off >>= 1)
+#pragma unroll
+      for (int gh = 0; gh < G; ++gh) part[0][gh] += __shfl_xor_sync(0xFFFFFFFFu, part[0][gh], off);
+
+    const bool my_valid = row0 + tok0 + my_row < end;
+    // running (m, l) per head, uniform over the group; the base only moves when the block
+    // maximum exceeds it by more than 2^8
+    float pw[G];
     bool grow_any = false;
     float corr[G];
 #pragma unroll
     for (int gh = 0; gh < G; ++gh) {
-      float mt = sc[0][gh];
+      const float sc = my_valid ? part[0][gh] : -INFINITY;
+      float mt = sc;
 #pragma unroll
-      for (int u = 1; u < Cfg::kPasses; ++u) mt = fmaxf(mt, sc[u][gh]);
+      for (int off = LPR / 2; off >= kRowLanes; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, off));
       const float m_cand = fmaxf(m[gh], mt);
       const bool grow = m_cand > m[gh] + kDecodeRescaleThreshold;
       corr[gh] = 1.f;
@@ -257,13 +294,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
       }
       grow_any |= grow;
       const float base = (m[gh] == -INFINITY) ? 0.f : m[gh];
-      float sum = 0.f;
-#pragma unroll
-      for (int u = 0; u < Cfg::kPasses; ++u) {
-        pw[u][gh] = ex2_approx(sc[u][gh] - base);
-        sum += pw[u][gh];
-      }
-      l[gh] = l[gh] * corr[gh] + sum;
+      pw[gh] = ex2_approx(sc - base);
+      l[gh] = l[gh] * corr[gh] + pw[gh];
     }
     if (__any_sync(0xFFFFFFFFu, grow_any)) {
 #pragma unroll
@@ -277,16 +309,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
         }
       }
     }
-    // o += p v over this lane group's rows
+    // o += p v over the group's rows (p of row u comes from its owner lanes)
 #pragma unroll
-    for (int u = 0; u < Cfg::kPasses; ++u) {
-      const int tok = warp * Cfg::kTokPerWarp + u * Cfg::kTokPerPass + grp;
-      if (row0 + tok < end) {
+    for (int u = 0; u < R; ++u) {
+      float pu[G];
+#pragma unroll
+      for (int gh = 0; gh < G; ++gh)
+        pu[gh] = __shfl_sync(0xFFFFFFFFu, pw[gh], grp_lane0 + u * kRowLanes + (sub % kRowLanes));
+      if (row0 + tok0 + u < end) {
         float vf[E];
-        load_row_chunks<D, EB>(vt + tok * Cfg::kRowBytes, sub, vf);
+        load_row_chunks<D, EB>(vt + (tok0 + u) * Cfg::kRowBytes, sub, vf);
 #pragma unroll
         for (int gh = 0; gh < G; ++gh) {
-          const float2 p2 = make_float2(pw[u][gh], pw[u][gh]);
+          const float2 p2 = make_float2(pu[gh], pu[gh]);
 #pragma unroll
           for (int e = 0; e < E; e += 2) {
             const float2 r = __ffma2_rn(p2, make_float2(vf[e], vf[e + 1]), make_float2(o[gh][e], o[gh][e + 1]));
@@ -300,6 +335,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     if (lane == 0) mbar_arrive(&empty_bar[s]);
   }
   __syncwarp();
+
+  // l: each lane summed the p of its own rows; add the group's distinct rows (the lanes
+  // that differ in the row-selecting bits), so every lane of the group holds the group's l
+#pragma unroll
+  for (int off = LPR / 2; off >= kRowLanes; off >>= 1)
+#pragma unroll
+    for (int gh = 0; gh < G; ++gh) l[gh] += __shfl_xor_sync(0xFFFFFFFFu, l[gh], off);
 
   // merge the lane groups of this warp (same chunks `sub`, different rows)
 #pragma unroll
