@@ -34,7 +34,7 @@ from .attention import (  # noqa: F401
     decode_split_merge,
     count_blocks,
 )
-from .rmsnorm import rmsnorm, rmsnorm_rows  # noqa: F401
+from .rmsnorm import rmsnorm, rmsnorm_rows, rmsnorm_residual  # noqa: F401
 from .fp8 import (  # noqa: F401
     E4M3_MAX,
     e4m3_value,

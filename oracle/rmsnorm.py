@@ -7,6 +7,12 @@ square root and the mean runs over the D axis of each row.
 Source: "Module 07: Fused operators and FlashAttention", section "Fused
 RMSNorm" (the formula) and section "Assignment 07.1: fused_rms_norm" (eps
 under the root, mean over D, not over T).
+
+The residual form (same module, the end of the RMSNorm assignment: the kernel
+also folds in the residual add, rms_norm(x + residual), saving one more pass):
+h = x + r (the new residual stream) and y = RMSNorm(h) * w, both from the exact
+sum. How the GPU splits the row's sum of squares ("Chapter 5. Operators and
+runtime", section 5.2.4) changes only the rounding, not this definition.
 """
 from __future__ import annotations
 
@@ -24,3 +30,9 @@ def rmsnorm_rows(x: np.ndarray, w: np.ndarray, eps: float, rows) -> np.ndarray:
     """The same definition evaluated for selected rows only."""
     rows = np.asarray(rows, dtype=np.int64)
     return rmsnorm(np.asarray(x)[rows], w, eps)
+
+
+def rmsnorm_residual(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float):
+    """x, r: [T, D], w: [D] -> (y, h): h = x + r, y = RMSNorm(h) * w (float64)."""
+    h = np.asarray(x, dtype=np.float64) + np.asarray(r, dtype=np.float64)
+    return rmsnorm(h, w, eps), h

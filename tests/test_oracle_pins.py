@@ -376,3 +376,22 @@ def test_rmsnorm_does_not_mutate_inputs():
     x0, w0 = x.copy(), w.copy()
     oracle.rmsnorm(x, w, 1e-6)
     assert np.array_equal(x, x0) and np.array_equal(w, w0)
+
+
+def test_rmsnorm_residual_reduces_to_rmsnorm_and_to_closed_forms():
+    # r = 0: exactly the plain RMSNorm; the sum is symmetric in x and r
+    x, r = _rand((5, 64), 47), _rand((5, 64), 48)
+    w = _rand((64,), 49)
+    y0, h0 = oracle.rmsnorm_residual(x, np.zeros_like(x), w, 1e-6)
+    assert np.array_equal(y0, oracle.rmsnorm(x, w, 1e-6)) and np.array_equal(h0, x)
+    y1, h1 = oracle.rmsnorm_residual(x, r, w, 1e-6)
+    y2, h2 = oracle.rmsnorm_residual(r, x, w, 1e-6)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+    # x = -r cancels: h = 0 and y = 0 (0 / sqrt(eps))
+    y3, h3 = oracle.rmsnorm_residual(x, -x, w, 1e-6)
+    assert np.array_equal(h3, np.zeros_like(x)) and np.array_equal(y3, np.zeros_like(x))
+    # constant rows again: x + r = c_t, y = c_t / sqrt(c_t^2 + eps) * w
+    c = np.array([0.25, -3.0])
+    xc = np.repeat((c / 2)[:, None], 16, axis=1)
+    yc, _ = oracle.rmsnorm_residual(xc, xc, np.ones(16), 1e-6)
+    assert np.allclose(yc, (c / np.sqrt(c * c + 1e-6))[:, None], rtol=0, atol=1e-14)
