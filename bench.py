@@ -315,6 +315,30 @@ def run_gpu(args):
             del xs, ys
         del flush
 
+    # ---- residual-add RMSNorm on the same X[4096, 1024] (h = bf16(x + r), y = RMSNorm(h) w): reads
+    #      x and r, writes h and y; L2 flushed before each launch
+    res_line = None
+    if not args.no_e2e:
+        flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+        rd = torch.randn(NORM.T, NORM.D, device=dev).to(torch.bfloat16)
+        hd = torch.empty_like(xd)
+        tms = []
+        for _ in range(8):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            attn.rmsnorm_residual(xd, rd, wd, eps=NORM.eps, out=yd, h=hd)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tms.append(a.elapsed_time(b))
+        tms.sort()
+        r_ms = max_over_ranks([tms[len(tms) // 2]], dev)[0]
+        r_bytes = 8 * NORM.T * NORM.D + 2 * NORM.D
+        res_line = {"value": round(r_bytes / (r_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "bound": "hbm",
+                    "peak": peaks["hbm"], "frac": round(r_bytes / (r_ms * 1e-3) / 1e9 / peaks["hbm"], 4),
+                    "us": round(1e3 * r_ms, 2), "bytes_per_launch": r_bytes, "workload": "X, R [4096, 1024]"}
+        del flush, rd, hd
+
     # ---- FP8 (E4M3) KV-cache decode on the same workload (its own timing, outside the step):
     #      the cache is quantised once on the GPU, then only the 1-byte codes are streamed
     dec8 = None
@@ -385,6 +409,7 @@ def run_gpu(args):
                         "frac": round(norm_gbs / peaks["hbm"], 4), "bytes_per_launch": norm_bytes,
                         "sweep_D1024": norm_sweep},
             "decode_fp8": dec8,
+            "rmsnorm_residual": res_line,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,

@@ -20,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "decode_workspace_size",
+__all__ = ["fwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
+           "decode_workspace_size",
            "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
 
@@ -228,6 +229,25 @@ def rmsnorm(x, w, eps: float = 1e-6, out=None, stream=None):
                                  _stream_ptr(stream))
     _lib.check("rmsnorm_fwd", st)
     return out
+
+
+def rmsnorm_residual(x, r, w, eps: float = 1e-6, out=None, h=None, stream=None):
+    """h = bf16(x + r) and y = RMSNorm(h) * w in one pass; returns (y, h).
+    ``h`` may be ``x`` or ``r`` (in-place update of the residual stream)."""
+    _check_tensor("x", x, torch.bfloat16, 2)
+    _check_tensor("r", r, torch.bfloat16, 2)
+    _check_tensor("w", w, torch.bfloat16, 1)
+    T, D = x.shape
+    if r.shape != x.shape or w.shape[0] != D:
+        raise ValueError("r must match x and w must have D elements")
+    if out is None:
+        out = torch.empty_like(x)
+    if h is None:
+        h = torch.empty_like(x)
+    st = _lib.load().rmsnorm_residual_fwd(x.data_ptr(), r.data_ptr(), w.data_ptr(), out.data_ptr(), h.data_ptr(),
+                                          T, D, float(eps), _stream_ptr(stream))
+    _lib.check("rmsnorm_residual_fwd", st)
+    return out, h
 
 
 def last_device_error(stream=None) -> int:

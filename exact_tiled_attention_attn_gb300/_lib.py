@@ -34,6 +34,7 @@ SIGNATURES = {
     "attn_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, ctypes.c_size_t,
                              _P]),
     "rmsnorm_fwd": (_I, [_P, _P, _P, _I, _I, _F, _P]),
+    "rmsnorm_residual_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _F, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_device_error": (_I, [_P]),
     "attn_kernel_launches": (ctypes.c_ulonglong, []),

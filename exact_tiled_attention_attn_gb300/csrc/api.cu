@@ -15,7 +15,9 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const f
                           float scale, int S, int C, void* workspace, cudaStream_t stream, int* launched);
 cudaError_t launch_kv_quantize_fp8(const void* x, void* codes, float* scale, int BH, long long per_head,
                                    cudaStream_t stream, int* launched);
-cudaError_t launch_rmsnorm(const void* x, const void* w, void* y, int T, int D, float eps, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void* x, const void* r, const void* w, void* y, void* h, int T, int D, float eps,
+                           cudaStream_t s);
+int rmsnorm_segments(int D);
 size_t decode_noalloc_capacity();
 cudaError_t decode_noalloc_scratch(void** ptr);
 uint32_t prefill_take_device_error();
@@ -182,9 +184,23 @@ attn_status rmsnorm_fwd(const void* x, const void* w, void* y, int T, int D, flo
   if (x == nullptr || w == nullptr || y == nullptr) return ATTN_ERR_INVALID_ARG;
   if (T < 1 || D < 8 || D % 8 != 0) return ATTN_ERR_INVALID_ARG;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID_ARG;
-  if (D > 8192) return ATTN_ERR_UNSUPPORTED;
+  if (rmsnorm_segments(D) == 0) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return ATTN_ERR_MISALIGNED;
-  const cudaError_t err = launch_rmsnorm(x, w, y, T, D, eps, stream);
+  const cudaError_t err = launch_rmsnorm(x, nullptr, w, y, nullptr, T, D, eps, stream);
+  if (err != cudaSuccess) return ATTN_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+attn_status rmsnorm_residual_fwd(const void* x, const void* r, const void* w, void* y, void* h, int T, int D,
+                                 float eps, cudaStream_t stream) {
+  if (x == nullptr || r == nullptr || w == nullptr || y == nullptr || h == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (T < 1 || D < 8 || D % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return ATTN_ERR_INVALID_ARG;
+  if (y == x || y == r || y == h) return ATTN_ERR_INVALID_ARG;
+  if (rmsnorm_segments(D) == 0) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(r) || !aligned16(w) || !aligned16(y) || !aligned16(h)) return ATTN_ERR_MISALIGNED;
+  const cudaError_t err = launch_rmsnorm(x, r, w, y, h, T, D, eps, stream);
   if (err != cudaSuccess) return ATTN_ERR_CUDA;
   g_launches.fetch_add(1);
   return ATTN_OK;

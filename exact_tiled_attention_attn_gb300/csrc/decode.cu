@@ -237,12 +237,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     const int row0 = start + t * Cfg::kTile;
     const int tok0 = warp * Cfg::kTokPerWarp + grp * R;  // first row of this group in the tile
 
-    // partial dot products of (c q) with this lane's 8 elements of each of the R rows
+    // partial dot products of (c q) with this lane's 8 elements of each of the R rows, taken
+    // in the order u ^ my_row: then at every step of the transpose-reduce below a lane keeps
+    // the first half of what it holds and sends the second half
     float part[R][G];
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       float kf[E];
-      load_row_chunks<D, EB>(kt + (tok0 + u) * Cfg::kRowBytes, sub, kf);  // rows past `end`: masked below
+      load_row_chunks<D, EB>(kt + (tok0 + (u ^ my_row)) * Cfg::kRowBytes, sub, kf);  // rows past `end`: masked below
 #pragma unroll
       for (int gh = 0; gh < G; ++gh) {
         float2 acc = make_float2(0.f, 0.f);
@@ -252,19 +254,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
         part[u][gh] = acc.x + acc.y;
       }
     }
-    // transpose-reduce: at lane distance `off` the lanes with that bit set keep the upper
-    // half of their rows and receive their partner's partial sums for it
+    // transpose-reduce: at lane distance `off` a lane keeps part[0 .. cnt) and receives its
+    // partner's partial sums for the same rows (the partner's row order differs in that bit)
 #pragma unroll
     for (int off = LPR / 2, cnt = R / 2; cnt >= 1; off >>= 1, cnt >>= 1) {
-      const bool upper = (sub & off) != 0;
 #pragma unroll
       for (int j = 0; j < cnt; ++j) {
 #pragma unroll
-        for (int gh = 0; gh < G; ++gh) {
-          const float keep = upper ? part[j + cnt][gh] : part[j][gh];
-          const float give = upper ? part[j][gh] : part[j + cnt][gh];
-          part[j][gh] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, off);
-        }
+        for (int gh = 0; gh < G; ++gh) part[j][gh] += __shfl_xor_sync(0xFFFFFFFFu, part[j + cnt][gh], off);
       }
     }
     // the lanes that share a row finish its sum
@@ -274,30 +271,38 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
       for (int gh = 0; gh < G; ++gh) part[0][gh] += __shfl_xor_sync(0xFFFFFFFFu, part[0][gh], off);
 
     const bool my_valid = row0 + tok0 + my_row < end;
-    // running (m, l) per head, uniform over the group; the base only moves when the block
-    // maximum exceeds it by more than 2^8
-    float pw[G];
-    bool grow_any = false;
-    float corr[G];
+    // running (m, l) per head, uniform over the group; the base only moves when a score
+    // exceeds it by more than 2^8, and only then is the block maximum over the group's rows
+    // formed (with shuffles); otherwise p = 2^(s - m) <= 2^8 with the base unchanged
+    float sc[G], pw[G], corr[G];
+    bool need = false;
 #pragma unroll
     for (int gh = 0; gh < G; ++gh) {
-      const float sc = my_valid ? part[0][gh] : -INFINITY;
-      float mt = sc;
-#pragma unroll
-      for (int off = LPR / 2; off >= kRowLanes; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, off));
-      const float m_cand = fmaxf(m[gh], mt);
-      const bool grow = m_cand > m[gh] + kDecodeRescaleThreshold;
+      sc[gh] = my_valid ? part[0][gh] : -INFINITY;
+      need |= sc[gh] > m[gh] + kDecodeRescaleThreshold;
       corr[gh] = 1.f;
-      if (grow) {
-        corr[gh] = ex2_approx(m[gh] - m_cand);  // 0 when m was -inf
-        m[gh] = m_cand;
+    }
+    const bool grow_any = __any_sync(0xFFFFFFFFu, need);
+    if (grow_any) {
+#pragma unroll
+      for (int gh = 0; gh < G; ++gh) {
+        float mt = sc[gh];
+#pragma unroll
+        for (int off = LPR / 2; off >= kRowLanes; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, off));
+        const float m_cand = fmaxf(m[gh], mt);
+        if (m_cand > m[gh] + kDecodeRescaleThreshold) {
+          corr[gh] = ex2_approx(m[gh] - m_cand);  // 0 when m was -inf
+          m[gh] = m_cand;
+        }
       }
-      grow_any |= grow;
+    }
+#pragma unroll
+    for (int gh = 0; gh < G; ++gh) {
       const float base = (m[gh] == -INFINITY) ? 0.f : m[gh];
-      pw[gh] = ex2_approx(sc - base);
+      pw[gh] = ex2_approx(sc[gh] - base);
       l[gh] = l[gh] * corr[gh] + pw[gh];
     }
-    if (__any_sync(0xFFFFFFFFu, grow_any)) {
+    if (grow_any) {
 #pragma unroll
       for (int gh = 0; gh < G; ++gh) {
         const float2 c2 = make_float2(corr[gh], corr[gh]);

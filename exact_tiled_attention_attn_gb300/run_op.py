@@ -6,6 +6,7 @@ mean CUDA-event time of the launches after the first.
 
   python -m exact_tiled_attention_attn_gb300.run_op --op prefill --workload gqa-llama --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op decode --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op decode_fp8 --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op rmsnorm --iters 3
 
 Workloads (seeded N(0,1) bf16 inputs):
@@ -32,7 +33,7 @@ PREFILL_WORKLOADS = {"single-head": "SINGLE_HEAD", "mha-gpt2": "MHA_GPT2", "gqa-
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["prefill", "decode", "rmsnorm"], required=True)
+    ap.add_argument("--op", choices=["prefill", "decode", "decode_fp8", "rmsnorm"], required=True)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--splits", type=int, default=0)
@@ -56,7 +57,7 @@ def main(argv=None):
         def run():
             attn.fwd(q, k, v, causal=shp.causal, scale=shp.scale, out=o, lse=lse)
         work, unit = shp.flops() / 1e12, "TFLOP/s"
-    elif args.op == "decode":
+    elif args.op in ("decode", "decode_fp8"):
         shp = W.DECODE_LLAMA
         q, kc, vc, sl = W.decode_inputs(shp)
         q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
@@ -64,10 +65,18 @@ def main(argv=None):
         ws = torch.empty(attn.decode_workspace_size(shp.B, shp.Hq, shp.d, S), dtype=torch.uint8, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty(shp.B, shp.Hq, dtype=torch.float32, device=dev)
+        if args.op == "decode":
+            def run():
+                attn.decode(q, kc, vc, sld, scale=shp.scale, num_splits=S, workspace=ws, out=o, lse=lse)
+            work, unit = 4 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (KV stream)"
+        else:  # the cache quantised to E4M3 once, outside the timed launches
+            kq, ks = attn.kv_quantize_fp8(kc)
+            vq, vs = attn.kv_quantize_fp8(vc)
+            del kc, vc
 
-        def run():
-            attn.decode(q, kc, vc, sld, scale=shp.scale, num_splits=S, workspace=ws, out=o, lse=lse)
-        work, unit = 4 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (KV stream)"
+            def run():
+                attn.decode_fp8(q, kq, vq, ks, vs, sld, scale=shp.scale, num_splits=S, workspace=ws, out=o, lse=lse)
+            work, unit = 2 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (E4M3 KV stream)"
     else:
         shp = W.NORM_QWEN
         x, w = W.norm_inputs(shp)

@@ -208,15 +208,40 @@ attn_status attn_decode_fp8(const void* q, const void* kcache, const void* vcach
  *
  * Defined by: "Module 07: Fused operators and FlashAttention", section
  * "Fused RMSNorm" (the formula; sum of squares kept in registers, the row
- * held by one warp, no x^2 tensor) and section "Assignment 07.1:
+ * held on chip, no x^2 tensor) and section "Assignment 07.1:
  * fused_rms_norm" (eps under the root, mean over D).
  *
  *   x  bf16 [T, D], w bf16 [D], y bf16 [T, D] (written; may not alias x)
- *   D  a multiple of 8, 8 <= D <= 8192; T >= 1; eps >= 0 and finite
- * Arithmetic: fp32 sum of squares and scaling, y rounded once to bf16.
+ *   D  a multiple of 8, 8 <= D <= 8192, and a multiple of 64 when D > 4096;
+ *   T >= 1; eps >= 0 and finite. All pointers 16-byte aligned.
+ * Arithmetic: fp32 sum of squares and scaling, y rounded once to bf16. The
+ * sum of squares follows one fixed order that depends only on D (8 segments
+ * of D/8 elements when D % 64 == 0, combined in a fixed tree; "Chapter 5.
+ * Operators and runtime", section 5.2.4), whatever T is and however the rows
+ * are spread over the GPU, so a row's y is bitwise independent of the batch
+ * it is normalised in.
  */
 attn_status rmsnorm_fwd(const void* x, const void* w, void* y, int T, int D, float eps,
                         cudaStream_t stream);
+
+/*
+ * rmsnorm_residual_fwd - the residual add fused into RMSNorm:
+ *   h = bf16(x + r)             (the new residual stream, written)
+ *   y = h / sqrt(mean_j h_j^2 + eps) * w
+ *
+ * Defined by: "Module 07: Fused operators and FlashAttention", end of the
+ * RMSNorm assignment (the kernel also folds in the residual add,
+ * rms_norm(x + residual), saving a pass). The norm reads the stored (bf16)
+ * h, as the unfused add-then-normalise pair would ("Chapter 5. Operators and
+ * runtime", section 5.4.3: fusion keeps the original rounding).
+ *
+ *   x, r  bf16 [T, D]; w bf16 [D]; y, h bf16 [T, D] (written)
+ *   h may alias x or r (in-place update of the residual stream); y must not
+ *   alias x, r or h. D, T, eps, alignment and the fixed order of the sum of
+ *   squares as rmsnorm_fwd.
+ */
+attn_status rmsnorm_residual_fwd(const void* x, const void* r, const void* w, void* y, void* h,
+                                 int T, int D, float eps, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* attn_status_string(attn_status s);

@@ -101,6 +101,39 @@ def test_rmsnorm_rejects_invalid_arguments(lib, args, code):
     assert lib.rmsnorm_fwd(*args, None) == code
 
 
+def test_rmsnorm_supported_widths(lib):
+    # D > 4096 must be a multiple of 64 (eight whole segments of 16-byte vectors)
+    assert lib.rmsnorm_fwd(FAKE, FAKE, FAKE, 4, 4104, 1e-6, None) == 2
+    assert lib.rmsnorm_fwd(FAKE, FAKE, FAKE, 4, 8200, 1e-6, None) == 2
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, FAKE, FAKE, FAKE, FAKE, 4, 1024, 1e-6), 1), ((FAKE, None, FAKE, FAKE, FAKE, 4, 1024, 1e-6), 1),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE + 64, 4, 1024, 1e-6), 1),  # y aliases x
+    ((FAKE, FAKE + 64, FAKE, FAKE + 128, FAKE + 128, 4, 1024, 1e-6), 1),  # y aliases h
+    ((FAKE, FAKE + 64, FAKE, FAKE + 128, FAKE + 192, 4, 4104, 1e-6), 2),
+    ((FAKE, FAKE + 72, FAKE, FAKE + 128, FAKE + 192, 4, 1024, 1e-6), 3),
+])
+def test_rmsnorm_residual_rejects_invalid_arguments(lib, args, code):
+    assert lib.rmsnorm_residual_fwd(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, FAKE, FAKE, 2, 4, 64, 128), 1), ((FAKE, FAKE, FAKE, 0, 4, 64, 128), 1),
+    ((FAKE, FAKE, FAKE, 2, 4, 64, 12), 2), ((FAKE, FAKE, FAKE, 300, 300, 64, 128), 2),
+    ((FAKE + 8, FAKE, FAKE, 2, 4, 64, 128), 3), ((FAKE, FAKE + 4, FAKE, 2, 4, 64, 128), 3),
+])
+def test_kv_quantize_rejects_invalid_arguments(lib, args, code):
+    assert lib.attn_kv_quantize_fp8(*args, None) == code
+
+
+def test_decode_fp8_needs_scales(lib):
+    args = [FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 256, 0.1, 2, FAKE, 1 << 20, None]
+    assert lib.attn_decode_fp8(*args) == 1
+    args[3], args[4] = FAKE, FAKE + 2
+    assert lib.attn_decode_fp8(*args) == 3
+
+
 def test_selftest_rejects_out_of_range_bound(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == 1
     assert lib.attn_selftest_wait_timeout(2_000_000, None) == 1

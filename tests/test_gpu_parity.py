@@ -350,6 +350,52 @@ def test_rmsnorm_special_inputs(attn):
     assert np.abs(np.sqrt((yr ** 2).mean(axis=1)) - 1).max() < 1e-2
 
 
+@pytest.mark.parametrize("D", [1024, 4096, 8192, 1000, 64])
+def test_rmsnorm_batch_invariant(attn, D):
+    # the same rows normalised alone (one block per row), in a batch of 512 (same shape) and in
+    # batches of 513 and 1030 (a warp per row) must agree bit for bit
+    gen = torch.Generator().manual_seed(70 + D)
+    x = (torch.randn(1030, D, generator=gen) * 3).to(torch.bfloat16).to(DEV)
+    w = (torch.rand(D, generator=gen) + 0.5).to(torch.bfloat16).to(DEV)
+    full = attn.rmsnorm(x, w, eps=1e-6)
+    part = attn.rmsnorm(x[:513].contiguous(), w, eps=1e-6)
+    small = attn.rmsnorm(x[:512].contiguous(), w, eps=1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(full[:513], part) and torch.equal(full[:512], small)
+    for i in (0, 5, 511, 512, 1029):
+        one = attn.rmsnorm(x[i:i + 1].contiguous(), w, eps=1e-6)
+        assert torch.equal(one[0], full[i]), f"row {i} differs when normalised alone"
+    assert_norm_close(full, oracle.rmsnorm(f64(x), f64(w), 1e-6), f"D{D}")
+
+
+def _bf16_round(v):
+    # round-to-nearest-even to bf16 of float64 values (8 significant bits), from frexp
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+@pytest.mark.parametrize("T,D", [(1, 4096), (7, 1024), (600, 1024), (4096, 1024), (33, 8192), (300, 1000)])
+def test_rmsnorm_residual(attn, T, D):
+    gen = torch.Generator().manual_seed(80 + T + D)
+    x = torch.randn(T, D, generator=gen).to(torch.bfloat16)
+    r = (torch.randn(T, D, generator=gen) * 0.5).to(torch.bfloat16)
+    w = (torch.rand(D, generator=gen) + 0.5).to(torch.bfloat16)
+    y, h = attn.rmsnorm_residual(x.to(DEV), r.to(DEV), w.to(DEV), eps=1e-6)
+    torch.cuda.synchronize()
+    Y, H = oracle.rmsnorm_residual(f64(x), f64(r), f64(w), 1e-6)
+    # h is the exact sum rounded once to bf16
+    assert np.array_equal(f64(h), _bf16_round(H))
+    assert_norm_close(y, Y, f"residual T{T} D{D}")
+    # in place: h written over r gives the same y and h
+    rd = r.to(DEV)
+    y2, h2 = attn.rmsnorm_residual(x.to(DEV), rd, w.to(DEV), eps=1e-6, h=rd)
+    torch.cuda.synchronize()
+    assert h2.data_ptr() == rd.data_ptr()
+    assert torch.equal(y2, y) and torch.equal(rd, h)
+    # the normalisation equals rmsnorm of the stored h, bit for bit (same fixed order)
+    assert torch.equal(attn.rmsnorm(h, w.to(DEV), eps=1e-6), y)
+
+
 # ----------------------------------------------------------------------------- failure path
 
 def test_bounded_wait_reports_timeout_and_context_survives(attn):
