@@ -369,6 +369,53 @@ def run_gpu(args):
                 "num_splits": splits}
         del kq, vq
 
+    # ---- short-context decode (B16 Hq32 Hkv8 d128, L ~ U[1024, 2048]): launch overhead is visible here;
+    #      20 steps launched one by one vs the same 20 steps captured once in a CUDA graph and replayed
+    short = None
+    if not args.no_e2e:
+        sshp = W.DecodeShape("short", DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.d, 1024, 2048, DECODE.seed)
+        sq, skc, svc, ssl = [t.to(dev) for t in W.decode_inputs(sshp)]
+        sS = attn.default_splits(sshp.B, sshp.Hkv, sshp.Lcap)
+        sws = torch.empty(attn.decode_workspace_size(sshp.B, sshp.Hq, sshp.d, sS), dtype=torch.uint8, device=dev)
+        so, sl_ = torch.empty_like(sq), torch.empty(sshp.B, sshp.Hq, dtype=torch.float32, device=dev)
+        nstep = 20
+
+        def short_steps():
+            for _ in range(nstep):
+                attn.decode(sq, skc, svc, ssl, scale=sshp.scale, num_splits=sS, workspace=sws, out=so, lse=sl_)
+
+        for _ in range(3):
+            short_steps()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record(stream)
+        short_steps()
+        b.record(stream)
+        torch.cuda.synchronize()
+        host_eager = (time.perf_counter() - t0) / nstep
+        eager_ms = a.elapsed_time(b) / nstep
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            short_steps()
+        g.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        host_graph = (time.perf_counter() - t0) / nstep
+        graph_ms = a.elapsed_time(b) / nstep
+        s_bytes = 4 * sshp.Hkv * sshp.d * int(ssl.sum().item())
+        short = {"workload": "flash-decoding B16 Hq32 Hkv8 d128 L~U[1024,2048]", "num_splits": sS,
+                 "eager_us_per_step": round(1e3 * eager_ms, 2), "graph_us_per_step": round(1e3 * graph_ms, 2),
+                 "eager_GB/s": round(s_bytes / (eager_ms * 1e-3) / 1e9, 1),
+                 "graph_GB/s": round(s_bytes / (graph_ms * 1e-3) / 1e9, 1),
+                 "host_wall_us_per_step_eager": round(1e6 * host_eager, 2),
+                 "host_wall_us_per_step_graph": round(1e6 * host_graph, 2)}
+        del g, sq, skc, svc, sws
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_heads)
@@ -410,6 +457,7 @@ def run_gpu(args):
                         "sweep_D1024": norm_sweep},
             "decode_fp8": dec8,
             "rmsnorm_residual": res_line,
+            "decode_short_context": short,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,

@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
     }
   }
   __syncthreads();
+  // this CTA's partials are written: the combine grid (launched with programmatic stream
+  // serialisation) may be scheduled once every CTA got here or exited; it still waits for
+  // this grid's completion before reading them (griddepcontrol.wait)
+  asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // One CTA per (sequence, query head): the weights 2^(m_s - M) of the non-empty splits
@@ -428,6 +432,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
   __shared__ float w_s[kMaxSplitsInSmem];
   __shared__ float red[D / 32];
   __shared__ float Ms, Ls;
+  // launched as a programmatic dependent of the split kernel: wait until that grid has
+  // completed and its writes are visible (a no-op without such a dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / Hq;
   int L = seqlens[b];
@@ -546,13 +553,28 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const f
                         : ((d == 64) ? launch_split_g<64, 2>(p, B, stream) : launch_split_g<128, 2>(p, B, stream));
   if (err != cudaSuccess) return err;
   *launched = 1;
+  // The combine is launched with programmatic stream serialisation: its grid can be set up
+  // while the split grid drains (launch overhead hidden), and griddepcontrol.wait in the
+  // kernel orders its reads after the split kernel's writes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(Hq));
+  cfg.blockDim = dim3(static_cast<unsigned>(d));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   if (d == 64) {
-    decode_combine_kernel<64><<<B * Hq, 64, 0, stream>>>(p.o_part, p.ml_part, seqlens,
-                                                         static_cast<__nv_bfloat16*>(o), lse, Hq, S, C, Lcap);
+    err = cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, static_cast<const float*>(p.o_part),
+                             static_cast<const float*>(p.ml_part), seqlens, ob, lse, Hq, S, C, Lcap);
   } else {
-    decode_combine_kernel<128><<<B * Hq, 128, 0, stream>>>(p.o_part, p.ml_part, seqlens,
-                                                           static_cast<__nv_bfloat16*>(o), lse, Hq, S, C, Lcap);
+    err = cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, static_cast<const float*>(p.o_part),
+                             static_cast<const float*>(p.ml_part), seqlens, ob, lse, Hq, S, C, Lcap);
   }
+  if (err != cudaSuccess) return err;
   err = cudaGetLastError();
   if (err == cudaSuccess) *launched = 2;
   return err;

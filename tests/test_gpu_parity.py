@@ -311,6 +311,41 @@ def test_decode_fp8_equals_bf16_decode_on_lossless_cache(attn):
     assert_attn_close(o8, l8, O, Lse, "lossless fp8 cache")
 
 
+def test_decode_and_prefill_replay_from_cuda_graphs(attn):
+    # the calls are capture-safe: captured once into CUDA graphs (the decode combine is a
+    # programmatic dependent of the split kernel), replays give the eager results bit for bit
+    shp = W.DecodeShape("t", 4, 8, 2, 128, 1, 1024, 33)
+    q, kc, vc, sl = [t.to(DEV) for t in W.decode_inputs(shp, seqlens=[1024, 5, 700, 333])]
+    kq, ks = attn.kv_quantize_fp8(kc)
+    vq, vs = attn.kv_quantize_fp8(vc)
+    S = 6
+    ws = torch.empty(attn.decode_workspace_size(4, 8, 128, S), dtype=torch.uint8, device=DEV)
+    ws8 = torch.empty_like(ws)
+    o_e, l_e = attn.decode(q, kc, vc, sl, num_splits=S, workspace=ws)
+    o8_e, l8_e = attn.decode_fp8(q, kq, vq, ks, vs, sl, num_splits=S, workspace=ws8)
+    pq, pk, pv = [t.to(DEV) for t in W.attention_inputs_custom(1, 4, 2, 300, 300, 128, 34)]
+    po_e, pl_e = attn.fwd(pq, pk, pv, causal=True)
+    o_g, l_g = torch.empty_like(o_e), torch.empty_like(l_e)
+    o8_g, l8_g = torch.empty_like(o8_e), torch.empty_like(l8_e)
+    po_g, pl_g = torch.empty_like(po_e), torch.empty_like(pl_e)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        attn.decode(q, kc, vc, sl, num_splits=S, workspace=ws, out=o_g, lse=l_g)
+        attn.decode_fp8(q, kq, vq, ks, vs, sl, num_splits=S, workspace=ws8, out=o8_g, lse=l8_g)
+        attn.fwd(pq, pk, pv, causal=True, out=po_g, lse=pl_g)
+    for _ in range(3):
+        o_g.zero_()
+        o8_g.zero_()
+        po_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e)
+        assert torch.equal(o8_g, o8_e) and torch.equal(l8_g, l8_e)
+        assert torch.equal(po_g, po_e) and torch.equal(pl_g, pl_e)
+    assert attn.last_device_error() == 0
+
+
 # ----------------------------------------------------------------------------- RMSNorm
 
 @pytest.mark.parametrize("T,D", [(1, 8), (37, 64), (300, 1000), (4096, 1024), (33, 4096), (5, 8192), (17, 2056)])
