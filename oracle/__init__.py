@@ -33,6 +33,7 @@ from .attention import (  # noqa: F401
     decode,
     decode_split_merge,
     count_blocks,
+    attention_backward,
 )
 from .rmsnorm import rmsnorm, rmsnorm_rows, rmsnorm_residual  # noqa: F401
 from .fp8 import (  # noqa: F401

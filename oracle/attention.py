@@ -20,6 +20,9 @@ Definitions followed (all in float64, bf16 inputs decoded exactly):
 * GQA: g = Hq / Hkv query heads share one K/V head; query head h reads K/V
   head floor(h / g) ("Attention from the kernel's side", section "Prefill and
   decoding are different problems", grouped-query attention).
+* Backward: the gradients by recomputation from the saved LSE ("FlashAttention:
+  attention without the n x n matrix", section "Backward pass: recomputing is
+  cheaper than storing"); see ``attention_backward``.
 * Decode: one query per sequence attends to keys 0 .. L_b - 1 of its cache;
   flash-decoding splits the key range, each split keeps a partial (m, l, o),
   and the partials are merged with the same rescaling rule (same section,
@@ -324,3 +327,41 @@ def decode_split_merge(q, kcache, vcache, seqlens, scale: float, num_splits: int
             O[b, h] = o / l
             L[b, h] = M + math.log(l)
     return O, L
+
+
+# ---------------------------------------------------------------------------
+# Backward pass by recomputation from the saved LSE
+# ---------------------------------------------------------------------------
+
+def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, lse: np.ndarray,
+                       do: np.ndarray, causal: bool, scale: float):
+    """Gradients of O = softmax(scale Q K^T + mask) V with respect to Q, K, V.
+
+    q, o, do: [B, Hq, Tq, d]; k, v: [B, Hkv, Tk, d]; lse: [B, Hq, Tq] (natural log, as
+    the forward returns it). Returns dQ [B, Hq, Tq, d], dK and dV [B, Hkv, Tk, d]; the
+    gradients of a K/V head are the sums over the g query heads that read it.
+    Source: "FlashAttention: attention without the n x n matrix", section "Backward
+    pass: recomputing is cheaper than storing": the scores are computed again, the
+    probabilities recovered without normalisation as P_ij = exp(S_ij - L_i), then
+    dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij - D_i) with D_i = dO_i . O_i,
+    dQ = dS K * scale, dK = dS^T Q * scale.
+    """
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    vis = _visible_mask(np.arange(Tq), Tk, causal)
+    for b in range(B):
+        for h in range(Hq):
+            kk, vv = k[b, h // g], v[b, h // g]
+            s = np.where(vis, (q[b, h] @ kk.T) * scale, NEG_INF)
+            p = np.exp(s - lse[b, h][:, None])
+            D = np.sum(do[b, h] * o[b, h], axis=1)
+            dv[b, h // g] += p.T @ do[b, h]
+            dp = do[b, h] @ vv.T
+            ds = p * (dp - D[:, None])
+            dq[b, h] = (ds @ kk) * scale
+            dk[b, h // g] += (ds.T @ q[b, h]) * scale
+    return dq, dk, dv

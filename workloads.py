@@ -139,6 +139,13 @@ def attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed, q_scale: float = 1.0):
     return q, k, v
 
 
+def grad_output(B, Hq, Tq, d, seed):
+    """The upstream gradient dO [B, Hq, Tq, d] for the backward pass: N(0,1) rounded to bf16,
+    from its own generator (seed + 7919, so it differs from the forward inputs' draws)."""
+    gen = torch.Generator().manual_seed(seed + 7919)
+    return _randn(gen, (B, Hq, Tq, d)).to(torch.bfloat16)
+
+
 def norm_inputs(shape: NormShape, T: int | None = None, seed: int | None = None):
     T = shape.T if T is None else T
     gen = torch.Generator().manual_seed(shape.seed if seed is None else seed)
