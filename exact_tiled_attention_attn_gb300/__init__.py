@@ -6,6 +6,7 @@ pointers, the current CUDA stream); every step of the computation runs in the
 library's CUDA kernels. PyTorch provides device memory and streams.
 
     o, lse = fwd(q, k, v, causal=True)             # q [B,Hq,T,d], k/v [B,Hkv,T,d], bf16
+    dq, dk, dv = bwd(q, k, v, o, lse, do, causal=True)
     o, lse = decode(q, kcache, vcache, seqlens)     # q [B,Hq,d], caches [B,Hkv,Lcap,d]
     y = rmsnorm(x, w, eps=1e-6)                     # x [T,D], w [D]
     codes, sc = kv_quantize_fp8(kcache)             # E4M3 codes (uint8) + fp32 scale per (b, head)
@@ -20,7 +21,7 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
+__all__ = ["fwd", "bwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
            "decode_workspace_size",
            "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
@@ -75,6 +76,38 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
                               B, Hq, Hkv, Tq, Tk, d, 1 if causal else 0, float(scale), _stream_ptr(stream))
     _lib.check("attn_fwd", st)
     return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of fwd's output with respect to q, k, v, given the upstream
+    gradient dout and the forward's o and lse (recomputation; bf16 in and out)."""
+    _check_tensor("q", q, torch.bfloat16, 4)
+    _check_tensor("k", k, torch.bfloat16, 4)
+    _check_tensor("v", v, torch.bfloat16, 4)
+    _check_tensor("o", o, torch.bfloat16, 4)
+    _check_tensor("dout", dout, torch.bfloat16, 4)
+    _check_tensor("lse", lse, torch.float32, 3)
+    B, Hq, Tq, d = q.shape
+    Hkv, Tk = k.shape[1], k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k and v must both be [B, Hkv, Tk, d] matching q")
+    if o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (B, Hq, Tq):
+        raise ValueError("o and dout must match q, lse must be [B, Hq, Tq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(_lib.load().attn_bwd_workspace_size(B, Hq, Tq))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = _lib.load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Tq, Tk, d,
+                              1 if causal else 0, float(scale), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _lib.check("attn_bwd", st)
+    return dq, dk, dv
 
 
 def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:

@@ -20,6 +20,10 @@ cudaError_t launch_rmsnorm(const void* x, const void* r, const void* w, void* y,
 int rmsnorm_segments(int D);
 size_t decode_noalloc_capacity();
 cudaError_t decode_noalloc_scratch(void** ptr);
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Tk,
+                            int d, int causal, float scale, void* workspace, cudaStream_t stream, int* launched);
+uint32_t backward_take_device_error();
 uint32_t prefill_take_device_error();
 uint32_t decode_take_device_error();
 uint32_t rmsnorm_take_device_error();
@@ -107,6 +111,37 @@ int attn_decode_default_splits(int B, int Hkv, int Lcap) {
   const int smax = (Lcap + 15) / 16;
   if (s > smax) s = smax;
   return s < 1 ? 1 : s;
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Tq) {
+  if (B < 1 || Hq < 1 || Tq < 1) return 0;
+  const size_t bytes = static_cast<size_t>(B) * Hq * Tq * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || dout == nullptr ||
+      dq == nullptr || dk == nullptr || dv == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > 65535 || static_cast<long long>(B) * Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < attn_bwd_workspace_size(B, Hq, Tq)) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  int launched = 0;
+  const cudaError_t err = launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, scale,
+                                          workspace, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status attn_decode(const void* q, const void* kcache, const void* vcache, const int* seqlens, void* o,
@@ -222,7 +257,7 @@ const char* attn_status_string(attn_status s) {
 attn_status attn_last_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
   const uint32_t e = prefill_take_device_error() | decode_take_device_error() | rmsnorm_take_device_error() |
-                     take_device_error_word();
+                     backward_take_device_error() | take_device_error_word();
   if (e == 0xFFFFFFFFu) return ATTN_ERR_CUDA;
   if (e & kErrTimeout) return ATTN_ERR_TIMEOUT;
   return ATTN_OK;

@@ -1,0 +1,559 @@
+// backward.cu - the attention backward pass on 5th-generation tensor cores (sm_103a).
+//
+// What it computes ("FlashAttention: attention without the n x n matrix", section
+// "Backward pass: recomputing is cheaper than storing"): from the forward's O and its
+// per-row log-sum-exp L, the scores of each block are computed again and the
+// probabilities recovered without normalisation, P_ij = exp(S_ij - L_i); then
+//   dV = P^T dO,  dP = dO V^T,  dS_ij = P_ij (dP_ij - D_i) with D_i = dO_i . O_i,
+//   dQ = dS K * scale,  dK = dS^T Q * scale.
+// With grouped-query attention the gradients of a K/V head are the sums over the g
+// query heads that read it.
+//
+// Three kernels, no atomics (every output is accumulated by one CTA):
+//   bwd_delta_kernel   D_i = dO_i . O_i, one warp per row (HBM-bound, fp32 into the workspace).
+//   bwd_dkdv_kernel    one CTA per (block of 128 keys, K/V head): walks the g query heads x
+//                      the visible query blocks; per block S^T = K Q^T and dP^T = V dO^T into
+//                      TMEM, 4 warps (one key row each) form P^T and dS^T (bf16) over the first
+//                      halves of those TMEM tiles, then dV += P^T dO and dK += dS^T Q with the
+//                      A operand from TMEM; dV and dK stay in TMEM until the end.
+//   bwd_dq_kernel      one CTA per (block of 128 queries, query head): walks the visible key
+//                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into TMEM, dQ += dS K.
+// Each kernel: warps 0-3 compute (TMEM lanes 0-127), warp 4 issues the TMA copies (two
+// stages of the walked operand pair), warp 5 issues the MMAs from one thread. Every
+// handoff is an mbarrier with a bounded wait; the steps of one block run one after the
+// other (recomputing S and dP in the dQ kernel costs 2 of its 3 GEMMs; the layout keeps
+// every output with one owner).
+//
+// P is rounded to bf16 for dV = P^T dO and dS to bf16 for the two gradient GEMMs; all
+// accumulation is fp32 in TMEM; outputs are rounded once to bf16.
+#include "common.cuh"
+
+namespace gb300 {
+
+constexpr uint64_t kBwdWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16 columns, 128-byte swizzle
+  static constexpr int kNumBox = D / 64;
+  static constexpr int kTileBytes = kNumBox * kBoxBytes;  // 128 rows x D
+  static constexpr int kThreads = 192;                    // warps 0-3 compute, 4 TMA, 5 MMA
+  // 2 resident tiles + 2 stages x 2 tiles; at least 116 KB so that one CTA runs per SM (each
+  // allocates all 512 TMEM columns)
+  static constexpr int kSmemBytes = (6 * kTileBytes + 1024) > 116 * 1024 ? (6 * kTileBytes + 1024) : 116 * 1024;
+  // [128 x 128] = A (128 x D, K-major) . B^T (B 128 x D, K-major)
+  static constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false);
+  // [128 x D] += A (TMEM, 128 x 128 bf16) . B (128 x D, MN-major)
+  static constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, D, true);
+  // TMEM columns: the two 128x128 fp32 score tiles, then the fp32 accumulators
+  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
+};
+
+struct BwdParams {
+  const float* lse;    // [B, Hq, Tq], natural log
+  const float* delta;  // [B, Hq, Tq]
+  __nv_bfloat16* dq;   // [B, Hq, Tq, D]
+  __nv_bfloat16* dk;   // [B, Hkv, Tk, D]
+  __nv_bfloat16* dv;
+  int B, Hq, Hkv, Tq, Tk, g, causal;
+  float c;             // scale * log2(e)
+  float scale;
+};
+
+// D[128 x 128] = A_tile . B_tile^T over K = D (both tiles 128 rows x D, K-major)
+template <int D>
+__device__ __forceinline__ void bwd_mma_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  using Cfg = BwdCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
+    umma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
+            Cfg::kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 x D] (+)= A (TMEM: 128 rows x 128 bf16, as 64 columns of pairs) . B (128 rows x D, MN-major)
+template <int D>
+__device__ __forceinline__ void bwd_mma_accumulate(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
+  using Cfg = BwdCfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk)  // 16 rows of B = 2048 bytes per step
+    umma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024), Cfg::kIdescAcc,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// One row (this thread's TMEM lane) of a [128 x D] fp32 accumulator, times `mul`, to bf16 in global.
+template <int D>
+__device__ __forceinline__ void bwd_store_row(uint32_t t_acc, float mul, bool have, bool store, __nv_bfloat16* dst) {
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t v[32];
+    if (have) {
+      tmem_ld32(t_acc + cc * 32, v);  // warp-collective: every lane runs it
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
+    if (store) {
+      uint4* o = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) o[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// D_i = dO_i . O_i
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, long long rows) {
+  constexpr int E = D / 32;  // elements per lane (2 or 4)
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const __nv_bfloat16* orow = o + row * D + lane * E;
+  const __nv_bfloat16* drow = dout + row * D + lane * E;
+  float acc = 0.f;
+  if constexpr (E == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(orow), b = *reinterpret_cast<const uint2*>(drow);
+    acc = fmaf(bf16lo_to_f32(a.x), bf16lo_to_f32(b.x), acc);
+    acc = fmaf(bf16hi_to_f32(a.x), bf16hi_to_f32(b.x), acc);
+    acc = fmaf(bf16lo_to_f32(a.y), bf16lo_to_f32(b.y), acc);
+    acc = fmaf(bf16hi_to_f32(a.y), bf16hi_to_f32(b.y), acc);
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(orow), b = *reinterpret_cast<const uint32_t*>(drow);
+    acc = fmaf(bf16lo_to_f32(a), bf16lo_to_f32(b), acc);
+    acc = fmaf(bf16hi_to_f32(a), bf16hi_to_f32(b), acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// ------------------------------------------------------------------------------------------
+// dK, dV: one CTA per (key block, K/V head)
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + Cfg::kTileBytes;
+  // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
+  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, p_ready, acc_done;
+  __shared__ float lse_s[128], dl_s[128];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+  const int j0 = blockIdx.x * 128;
+  const int n_qb = (p.Tq + 127) / 128;
+  // query blocks that see any key of this block (top-left causal: query q sees key j iff j <= q)
+  const int i_first = p.causal ? j0 / 128 : 0;
+  const int n_i = max(0, n_qb - i_first);
+  const int n_it = p.g * n_i;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&s_ready, 1);
+    mbar_init(&p_ready, 4);
+    mbar_init(&acc_done, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_it > 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmDO);
+      mbar_arrive_expect_tx(&kv_full, 2 * Cfg::kTileBytes);
+      for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
+        tma_load_3d(sK + kb * Cfg::kBoxBytes, &tmK, &kv_full, kb * 64, j0, b * p.Hkv + kvh);
+        tma_load_3d(sV + kb * Cfg::kBoxBytes, &tmV, &kv_full, kb * 64, j0, b * p.Hkv + kvh);
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !mbar_wait(&empty[s], static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+          break;
+        const int h = kvh * p.g + it / n_i;
+        const int i0 = (i_first + it % n_i) * 128;
+        uint8_t* sQ = smem + (2 + 2 * s) * Cfg::kTileBytes;
+        uint8_t* sDO = smem + (3 + 2 * s) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
+          tma_load_3d(sQ + kb * Cfg::kBoxBytes, &tmQ, &full[s], kb * 64, i0, b * p.Hq + h);
+          tma_load_3d(sDO + kb * Cfg::kBoxBytes, &tmDO, &full[s], kb * 64, i0, b * p.Hq + h);
+        }
+      }
+      if (*abort_p) {  // let copies still in flight land before the CTA exits
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it & 1;
+        const uint32_t aQ = smem_u32(smem + (2 + 2 * s) * Cfg::kTileBytes);
+        const uint32_t aDO = smem_u32(smem + (3 + 2 * s) * Cfg::kTileBytes);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>(it >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+        tc_fence_after();
+        bwd_mma_scores<D>(tmem + Cfg::kTmS, aK, aQ);    // S^T = K Q^T
+        bwd_mma_scores<D>(tmem + Cfg::kTmDP, aV, aDO);  // dP^T = V dO^T
+        umma_commit(&s_ready);
+        if (!mbar_wait(&p_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+        tc_fence_after();
+        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc0, tmem + Cfg::kTmS, aDO, it > 0);   // dV += P^T dO
+        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc1, tmem + Cfg::kTmDP, aQ, it > 0);   // dK += dS^T Q
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
+    }
+    __syncwarp();
+  } else {
+    // ---------------- compute warps: thread t owns key row j0 + t (TMEM lane t) ----------------
+    const int t = threadIdx.x;
+    const int key = j0 + t;
+    const bool key_ok = key < p.Tk;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.c;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = kvh * p.g + it / n_i;
+      const int i0 = (i_first + it % n_i) * 128;
+      named_bar_sync(1, 128);  // the previous block's readers of lse_s / dl_s are done
+      {
+        const int q = i0 + t;
+        const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + q;
+        lse_s[t] = q < p.Tq ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
+        dl_s[t] = q < p.Tq ? p.delta[r] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(it) & 1u, abort_p,
+                                                      kBwdWaitTimeoutNs));
+      if (ok) {
+        tc_fence_after();
+        // P^T and dS^T overwrite the first halves of their fp32 tiles: chunk cc writes columns
+        // [16cc, 16cc + 16), which chunks <= cc have already read
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tmem + lane_off + Cfg::kTmS + cc * 32, sr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmDP + cc * 32, dr);
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int qi = cc * 32 + 2 * k + e;
+              const bool vis = key_ok && (!p.causal || key <= i0 + qi);
+              pv[e] = vis ? ex2_approx(__uint_as_float(sr[2 * k + e]) * c - lse_s[qi]) : 0.f;
+              dv[e] = pv[e] * (__uint_as_float(dr[2 * k + e]) - dl_s[qi]);
+            }
+            pp[k] = pack_bf16x2(pv[0], pv[1]);
+            dd[k] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_st16(tmem + lane_off + Cfg::kTmS + cc * 16, pp);
+          tmem_st16(tmem + lane_off + Cfg::kTmDP + cc * 16, dd);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready);  // every block, also after a failed wait
+    }
+    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
+    tc_fence_after();
+    const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tk + key;
+    const bool have = ok && n_it > 0;
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, 1.f, have, key_ok && (ok || n_it == 0), p.dv + orow * D);
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc1, p.scale, have, key_ok && (ok || n_it == 0), p.dk + orow * D);
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dQ: one CTA per (query block, query head)
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + Cfg::kTileBytes;
+  // stage s: K at 2 + 2s, V at 3 + 2s (in tiles)
+  __shared__ uint64_t qd_full, full[2], empty[2], s_ready, p_ready, acc_done;
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
+  const int kvh = h / p.g;
+  const int i0 = blockIdx.x * 128;
+  const int n_kb = (p.Tk + 127) / 128;
+  const int last_row = min(i0 + 127, p.Tq - 1);
+  const int n_j = p.causal ? min(n_kb, last_row / 128 + 1) : n_kb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&qd_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&s_ready, 1);
+    mbar_init(&p_ready, 4);
+    mbar_init(&acc_done, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n_j > 0) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmDO);
+      mbar_arrive_expect_tx(&qd_full, 2 * Cfg::kTileBytes);
+      for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
+        tma_load_3d(sQ + kb * Cfg::kBoxBytes, &tmQ, &qd_full, kb * 64, i0, b * p.Hq + h);
+        tma_load_3d(sDO + kb * Cfg::kBoxBytes, &tmDO, &qd_full, kb * 64, i0, b * p.Hq + h);
+      }
+      for (int j = 0; j < n_j; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&empty[s], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+          break;
+        uint8_t* sK = smem + (2 + 2 * s) * Cfg::kTileBytes;
+        uint8_t* sV = smem + (3 + 2 * s) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
+          tma_load_3d(sK + kb * Cfg::kBoxBytes, &tmK, &full[s], kb * 64, j * 128, b * p.Hkv + kvh);
+          tma_load_3d(sV + kb * Cfg::kBoxBytes, &tmV, &full[s], kb * 64, j * 128, b * p.Hkv + kvh);
+        }
+      }
+      if (*abort_p) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
+      for (int j = 0; ok && j < n_j; ++j) {
+        const int s = j & 1;
+        const uint32_t aK = smem_u32(smem + (2 + 2 * s) * Cfg::kTileBytes);
+        const uint32_t aV = smem_u32(smem + (3 + 2 * s) * Cfg::kTileBytes);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>(j >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+        tc_fence_after();
+        bwd_mma_scores<D>(tmem + Cfg::kTmS, aQ, aK);    // S = Q K^T
+        bwd_mma_scores<D>(tmem + Cfg::kTmDP, aDO, aV);  // dP = dO V^T
+        umma_commit(&s_ready);
+        if (!mbar_wait(&p_ready, static_cast<uint32_t>(j) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+        tc_fence_after();
+        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc0, tmem + Cfg::kTmDP, aK, j > 0);  // dQ += dS K
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&acc_done);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- compute warps: thread t owns query row i0 + t (TMEM lane t) ----------------
+    const int t = threadIdx.x;
+    const int q = i0 + t;
+    const bool q_ok = q < p.Tq;
+    const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + (q_ok ? q : 0);
+    const float lse2 = q_ok ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
+    const float dl = q_ok ? p.delta[r] : 0.f;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.c;
+    bool ok = true;
+    for (int j = 0; j < n_j; ++j) {
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(j) & 1u, abort_p,
+                                                      kBwdWaitTimeoutNs));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tmem + lane_off + Cfg::kTmS + cc * 32, sr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmDP + cc * 32, dr);
+          uint32_t dd[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = j * 128 + cc * 32 + 2 * k + e;
+              const bool vis = key < p.Tk && (!p.causal || key <= q);
+              const float pv = vis ? ex2_approx(__uint_as_float(sr[2 * k + e]) * c - lse2) : 0.f;
+              dv[e] = pv * (__uint_as_float(dr[2 * k + e]) - dl);
+            }
+            dd[k] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_st16(tmem + lane_off + Cfg::kTmDP + cc * 16, dd);  // dS over the first half of dP
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready);
+    }
+    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
+    tc_fence_after();
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, p.scale, ok && n_j > 0, q_ok && (ok || n_j == 0),
+                     p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D);
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------
+typedef CUresult (*PFN_encodeTiledBwd)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiledBwd bwd_encode_fn() {
+  static PFN_encodeTiledBwd fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiledBwd>(ptr);
+  }
+  return fn;
+}
+
+// [Z, rows, D] bf16, box 64 columns x 128 rows x 1, 128-byte swizzle, rows past the end read as zero
+static bool bwd_map_3d(CUtensorMap* map, const void* base, int D, int rows, int Z) {
+  PFN_encodeTiledBwd enc = bwd_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(Z)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                const CUtensorMap& mdo, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                float* delta, const BwdParams& p, cudaStream_t stream, int* launched) {
+  using Cfg = BwdCfg<D>;
+  const long long rows = static_cast<long long>(p.B) * p.Hq * p.Tq;
+  bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(o, dout, delta, rows);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  *launched = 1;
+  err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const dim3 g_kv((p.Tk + 127) / 128, p.B * p.Hkv);
+  bwd_dkdv_kernel<D><<<g_kv, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  *launched = 2;
+  const dim3 g_q((p.Tq + 127) / 128, p.B * p.Hq);
+  bwd_dq_kernel<D><<<g_q, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  *launched = 3;
+  return cudaSuccess;
+}
+
+cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Tk,
+                            int d, int causal, float scale, void* workspace, cudaStream_t stream, int* launched) {
+  *launched = 0;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!bwd_map_3d(&mq, q, d, Tq, B * Hq) || !bwd_map_3d(&mk, k, d, Tk, B * Hkv) ||
+      !bwd_map_3d(&mv, v, d, Tk, B * Hkv) || !bwd_map_3d(&mdo, dout, d, Tq, B * Hq))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Tq = Tq;
+  p.Tk = Tk;
+  p.g = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.c = scale * kLog2e;
+  p.scale = scale;
+  const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(o);
+  const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dout);
+  float* delta = static_cast<float*>(workspace);
+  return d == 64 ? launch_bwd_d<64>(mq, mk, mv, mdo, ob, db, delta, p, stream, launched)
+                 : launch_bwd_d<128>(mq, mk, mv, mdo, ob, db, delta, p, stream, launched);
+}
+
+uint32_t backward_take_device_error() { return take_device_error_word(); }
+
+}  // namespace gb300

@@ -90,6 +90,34 @@ size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
 int attn_decode_default_splits(int B, int Hkv, int Lcap);
 
 /*
+ * attn_bwd - gradients of attn_fwd with respect to q, k and v, by recomputation
+ * from the forward's O and LSE.
+ *
+ * Defined by: "FlashAttention: attention without the n x n matrix", section
+ * "Backward pass: recomputing is cheaper than storing": the block scores are
+ * computed again, P_ij = exp(S_ij - L_i) without normalisation, then
+ * dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij - D_i) with D_i = dO_i . O_i,
+ * dQ = dS K * scale, dK = dS^T Q * scale. With Hq > Hkv the gradients of a
+ * K/V head are the sums over the Hq/Hkv query heads that read it.
+ *
+ *   q, o, dout  bf16 [B, Hq, Tq, d]; k, v bf16 [B, Hkv, Tk, d]
+ *   lse         fp32 [B, Hq, Tq]: the natural log-sum-exp attn_fwd returned
+ *   dq          bf16 [B, Hq, Tq, d] (written); dk, dv bf16 [B, Hkv, Tk, d] (written)
+ *   causal, scale, d, Hq % Hkv: as attn_fwd (the same causal rule, key j seen by
+ *   query i iff j <= i). B*Hq <= 65535.
+ *   workspace   device scratch of attn_bwd_workspace_size(B, Hq, Tq) bytes,
+ *               16-byte aligned, owned by the caller (holds D_i).
+ * Arithmetic: P and dS rounded to bf16 for the tensor-core products, fp32
+ * accumulation, outputs rounded once to bf16. Three kernel launches; the
+ * result does not depend on their timing (no atomics).
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Tq);
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv,
+                     int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_decode - one query token per sequence against a bf16 KV cache
  * (flash-decoding).
  *
