@@ -416,6 +416,40 @@ def run_gpu(args):
                  "host_wall_us_per_step_graph": round(1e6 * host_graph, 2)}
         del g, sq, skc, svc, sws
 
+    # ---- backward pass on the prefill workload (its own timing, outside the step). Algorithmic
+    #      FLOPs: the 5 GEMMs of the gradients, 2.5x the forward's (the kernels recompute S and
+    #      dP for dQ: 7 GEMMs executed)
+    bwd_line = None
+    if not args.no_bwd:
+        dod = W.grad_output(PREFILL.B, PREFILL.Hq, PREFILL.T, PREFILL.d, PREFILL.seed).to(dev)
+        gq, gk, gv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        bws = torch.empty(attn.lib().attn_bwd_workspace_size(PREFILL.B, PREFILL.Hq, PREFILL.T), dtype=torch.uint8,
+                          device=dev)
+        attn.fwd(qd, kd, vd, causal=True, scale=PREFILL.scale, out=od, lse=lsed)
+
+        def bwd_once():
+            attn.bwd(qd, kd, vd, od, lsed, dod, causal=True, scale=PREFILL.scale, dq=gq, dk=gk, dv=gv, workspace=bws)
+
+        for _ in range(3):
+            bwd_once()
+        torch.cuda.synchronize()
+        nb = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(nb):
+            bwd_once()
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert attn.last_device_error() == 0
+        b_ms = max_over_ranks([a.elapsed_time(b) / nb], dev)[0]
+        b_flops = 2.5 * flops
+        b_tf = b_flops / (b_ms * 1e-3) / 1e12
+        bwd_line = {"value": round(b_tf, 2), "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16"],
+                    "frac": round(b_tf / peaks["bf16"], 4), "ms": round(b_ms, 4), "flops_per_launch": b_flops,
+                    "workload": PREFILL.name,
+                    "kernels": "bwd_delta_kernel<128> + bwd_dkdv_kernel<128> + bwd_dq_kernel<128>"}
+        del dod, gq, gk, gv, bws
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_heads)
@@ -458,6 +492,7 @@ def run_gpu(args):
             "decode_fp8": dec8,
             "rmsnorm_residual": res_line,
             "decode_short_context": short,
+            "backward": bwd_line,
             "e2e": e2e,
             "gpu_launches": int(launches),
             "clocks": clocks,
@@ -584,6 +619,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV-cache decode line")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -13,13 +13,14 @@
 //   bwd_delta_kernel   D_i = dO_i . O_i, one warp per row (HBM-bound, fp32 into the workspace).
 //   bwd_dkdv_kernel    one CTA per (block of 128 keys, K/V head): walks the g query heads x
 //                      the visible query blocks; per block S^T = K Q^T and dP^T = V dO^T into
-//                      TMEM, 4 warps (one key row each) form P^T and dS^T (bf16) over the first
-//                      halves of those TMEM tiles, then dV += P^T dO and dK += dS^T Q with the
+//                      TMEM, 8 warps (two per key row) form P^T and dS^T (bf16) inside those
+//                      TMEM tiles, then dV += P^T dO and dK += dS^T Q with the
 //                      A operand from TMEM; dV and dK stay in TMEM until the end.
 //   bwd_dq_kernel      one CTA per (block of 128 queries, query head): walks the visible key
 //                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into TMEM, dQ += dS K.
-// Each kernel: warps 0-3 compute (TMEM lanes 0-127), warp 4 issues the TMA copies (two
-// stages of the walked operand pair), warp 5 issues the MMAs from one thread. Every
+// Each kernel: warps 0-7 compute (warps w and w + 4 share TMEM lanes 32(w mod 4) .. + 31 and
+// take one half of the row's 128 columns each), warp 8 issues the TMA copies (two stages of the
+// walked operand pair), warp 9 issues the MMAs from one thread. Every
 // handoff is an mbarrier with a bounded wait; the steps of one block run one after the
 // other (recomputing S and dP in the dQ kernel costs 2 of its 3 GEMMs; the layout keeps
 // every output with one owner).
@@ -38,7 +39,7 @@ struct BwdCfg {
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16 columns, 128-byte swizzle
   static constexpr int kNumBox = D / 64;
   static constexpr int kTileBytes = kNumBox * kBoxBytes;  // 128 rows x D
-  static constexpr int kThreads = 192;                    // warps 0-3 compute, 4 TMA, 5 MMA
+  static constexpr int kThreads = 320;                    // warps 0-7 compute, 8 TMA, 9 MMA
   // 2 resident tiles + 2 stages x 2 tiles; at least 116 KB so that one CTA runs per SM (each
   // allocates all 512 TMEM columns)
   static constexpr int kSmemBytes = (6 * kTileBytes + 1024) > 116 * 1024 ? (6 * kTileBytes + 1024) : 116 * 1024;
@@ -73,21 +74,26 @@ __device__ __forceinline__ void bwd_mma_scores(uint32_t d_tmem, uint32_t a_smem,
   }
 }
 
-// D[128 x D] (+)= A (TMEM: 128 rows x 128 bf16, as 64 columns of pairs) . B (128 rows x D, MN-major)
+// D[128 x D] (+)= A (TMEM: 128 rows x 128 bf16) . B (128 rows x D, MN-major). A's bf16 pairs sit
+// in two ranges of the 128-column tile they replaced: columns 0..63 of the tile at [0, 32),
+// columns 64..127 at [64, 96) (each half of the compute warps writes inside the columns it read).
 template <int D>
 __device__ __forceinline__ void bwd_mma_accumulate(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
   using Cfg = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)  // 16 rows of B = 2048 bytes per step
-    umma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024), Cfg::kIdescAcc,
-            (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(d_tmem, a_tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024),
+            Cfg::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// One row (this thread's TMEM lane) of a [128 x D] fp32 accumulator, times `mul`, to bf16 in global.
+// Half `half` (columns [half*D/2, (half+1)*D/2)) of one row (this thread's TMEM lane) of a
+// [128 x D] fp32 accumulator, times `mul`, to bf16 in global.
 template <int D>
-__device__ __forceinline__ void bwd_store_row(uint32_t t_acc, float mul, bool have, bool store, __nv_bfloat16* dst) {
+__device__ __forceinline__ void bwd_store_row(uint32_t t_acc, float mul, bool have, bool store, __nv_bfloat16* dst,
+                                              int half) {
 #pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
+  for (int c2 = 0; c2 < D / 64; ++c2) {
+    const int cc = half * (D / 64) + c2;
     uint32_t v[32];
     if (have) {
       tmem_ld32(t_acc + cc * 32, v);  // warp-collective: every lane runs it
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // dK, dV: one CTA per (key block, K/V head)
 // ------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams p) {
@@ -151,7 +157,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sV = smem + Cfg::kTileBytes;
   // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
   __shared__ uint64_t kv_full, full[2], empty[2], s_ready, p_ready, acc_done;
-  __shared__ float lse_s[128], dl_s[128];
+  __shared__ __align__(16) float lse_s[128];  // read as float4
+  __shared__ __align__(16) float dl_s[128];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
 
@@ -171,12 +178,12 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_ready, 1);
-    mbar_init(&p_ready, 4);
+    mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&tmem_holder, 512);
     tmem_relinquish();
   }
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = tmem_holder;
   volatile int* abort_p = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_it > 0) {
       prefetch_tensormap(&tmQ);
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
@@ -243,51 +250,60 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- compute warps: thread t owns key row j0 + t (TMEM lane t) ----------------
+    // ---------------- compute warps: key row j0 + (t & 127) (TMEM lane), query half t >> 7 ----------------
     const int t = threadIdx.x;
-    const int key = j0 + t;
+    const int row = t & 127, half = t >> 7;
+    const int key = j0 + row;
     const bool key_ok = key < p.Tk;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.c;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = kvh * p.g + it / n_i;
       const int i0 = (i_first + it % n_i) * 128;
-      named_bar_sync(1, 128);  // the previous block's readers of lse_s / dl_s are done
+      named_bar_sync(1, 256);  // the previous block's readers of lse_s / dl_s are done
       {
-        const int q = i0 + t;
+        const int q = i0 + row;
         const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + q;
-        lse_s[t] = q < p.Tq ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
-        dl_s[t] = q < p.Tq ? p.delta[r] : 0.f;
+        if (half == 0) lse_s[row] = q < p.Tq ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
+        else dl_s[row] = q < p.Tq ? p.delta[r] : 0.f;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(it) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
-        // P^T and dS^T overwrite the first halves of their fp32 tiles: chunk cc writes columns
-        // [16cc, 16cc + 16), which chunks <= cc have already read
+        // This half's 64 queries in two chunks of 32; chunk cc reads columns [q0, q0 + 32) and
+        // writes its bf16 pairs to [q0 / 2 + half * 32, + 16), inside the columns this half read
+        // and already consumed.
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int q0 = half * 64 + cc * 32;
           uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + Cfg::kTmS + cc * 32, sr);
-          tmem_ld32(tmem + lane_off + Cfg::kTmDP + cc * 32, dr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmS + q0, sr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmDP + q0, dr);
           uint32_t pp[16], dd[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float pv[2], dv[2];
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + 4 * v4);
+            const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + 4 * v4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], gv[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int qi = cc * 32 + 2 * k + e;
+            for (int e = 0; e < 4; ++e) {
+              const int qi = q0 + 4 * v4 + e;
               const bool vis = key_ok && (!p.causal || key <= i0 + qi);
-              pv[e] = vis ? ex2_approx(__uint_as_float(sr[2 * k + e]) * c - lse_s[qi]) : 0.f;
-              dv[e] = pv[e] * (__uint_as_float(dr[2 * k + e]) - dl_s[qi]);
+              pv[e] = vis ? ex2_approx(__uint_as_float(sr[4 * v4 + e]) * c - lv[e]) : 0.f;
+              gv[e] = pv[e] * (__uint_as_float(dr[4 * v4 + e]) - dvv[e]);
             }
-            pp[k] = pack_bf16x2(pv[0], pv[1]);
-            dd[k] = pack_bf16x2(dv[0], dv[1]);
+            pp[2 * v4] = pack_bf16x2(pv[0], pv[1]);
+            pp[2 * v4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dd[2 * v4] = pack_bf16x2(gv[0], gv[1]);
+            dd[2 * v4 + 1] = pack_bf16x2(gv[2], gv[3]);
           }
-          tmem_st16(tmem + lane_off + Cfg::kTmS + cc * 16, pp);
-          tmem_st16(tmem + lane_off + Cfg::kTmDP + cc * 16, dd);
+          const uint32_t out_col = half * 64 + cc * 16;
+          tmem_st16(tmem + lane_off + Cfg::kTmS + out_col, pp);
+          tmem_st16(tmem + lane_off + Cfg::kTmDP + out_col, dd);
         }
         tmem_st_wait();
       }
@@ -299,12 +315,13 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tk + key;
     const bool have = ok && n_it > 0;
-    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, 1.f, have, key_ok && (ok || n_it == 0), p.dv + orow * D);
-    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc1, p.scale, have, key_ok && (ok || n_it == 0), p.dk + orow * D);
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, 1.f, have, key_ok && (ok || n_it == 0), p.dv + orow * D, half);
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc1, p.scale, have, key_ok && (ok || n_it == 0), p.dk + orow * D,
+                     half);
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(192, 1)
 // dQ: one CTA per (query block, query head)
 // ------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
@@ -343,12 +360,12 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_ready, 1);
-    mbar_init(&p_ready, 4);
+    mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&tmem_holder, 512);
     tmem_relinquish();
   }
@@ -358,7 +375,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = tmem_holder;
   volatile int* abort_p = &abort_flag;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0 && n_j > 0) {
       prefetch_tensormap(&tmQ);
@@ -389,7 +406,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
@@ -412,14 +429,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- compute warps: thread t owns query row i0 + t (TMEM lane t) ----------------
+    // ---------------- compute warps: query row i0 + (t & 127) (TMEM lane), key half t >> 7 ----------------
     const int t = threadIdx.x;
-    const int q = i0 + t;
+    const int row = t & 127, half = t >> 7;
+    const int q = i0 + row;
     const bool q_ok = q < p.Tq;
     const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + (q_ok ? q : 0);
     const float lse2 = q_ok ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
     const float dl = q_ok ? p.delta[r] : 0.f;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.c;
     bool ok = true;
     for (int j = 0; j < n_j; ++j) {
@@ -427,25 +445,27 @@ __global__ void __launch_bounds__(192, 1)
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
+        // this half's 64 keys in two chunks of 32; dS pairs go inside the columns this half read
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
+          const int k0 = half * 64 + cc * 32;
           uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + Cfg::kTmS + cc * 32, sr);
-          tmem_ld32(tmem + lane_off + Cfg::kTmDP + cc * 32, dr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmS + k0, sr);
+          tmem_ld32(tmem + lane_off + Cfg::kTmDP + k0, dr);
           uint32_t dd[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             float dv[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int key = j * 128 + cc * 32 + 2 * k + e;
+              const int key = j * 128 + k0 + 2 * k + e;
               const bool vis = key < p.Tk && (!p.causal || key <= q);
               const float pv = vis ? ex2_approx(__uint_as_float(sr[2 * k + e]) * c - lse2) : 0.f;
               dv[e] = pv * (__uint_as_float(dr[2 * k + e]) - dl);
             }
             dd[k] = pack_bf16x2(dv[0], dv[1]);
           }
-          tmem_st16(tmem + lane_off + Cfg::kTmDP + cc * 16, dd);  // dS over the first half of dP
+          tmem_st16(tmem + lane_off + Cfg::kTmDP + half * 64 + cc * 16, dd);  // dS
         }
         tmem_st_wait();
       }
@@ -456,11 +476,11 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
     tc_fence_after();
     bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, p.scale, ok && n_j > 0, q_ok && (ok || n_j == 0),
-                     p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D);
+                     p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D, half);
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

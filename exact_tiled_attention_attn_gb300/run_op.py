@@ -5,6 +5,7 @@ chosen operation needs, runs it ``--iters`` times on cuda:0 and prints the
 mean CUDA-event time of the launches after the first.
 
   python -m exact_tiled_attention_attn_gb300.run_op --op prefill --workload gqa-llama --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op backward --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op decode --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op decode_fp8 --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op rmsnorm --iters 3
@@ -33,7 +34,7 @@ PREFILL_WORKLOADS = {"single-head": "SINGLE_HEAD", "mha-gpt2": "MHA_GPT2", "gqa-
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["prefill", "decode", "decode_fp8", "rmsnorm"], required=True)
+    ap.add_argument("--op", choices=["prefill", "backward", "decode", "decode_fp8", "rmsnorm"], required=True)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--splits", type=int, default=0)
@@ -57,6 +58,17 @@ def main(argv=None):
         def run():
             attn.fwd(q, k, v, causal=shp.causal, scale=shp.scale, out=o, lse=lse)
         work, unit = shp.flops() / 1e12, "TFLOP/s"
+    elif args.op == "backward":
+        shp = getattr(W, PREFILL_WORKLOADS[args.workload or "gqa-llama"])
+        q, k, v = W.attention_inputs(shp)[:3]
+        q, k, v = q.to(dev), k.to(dev), v.to(dev)
+        do = W.grad_output(shp.B, shp.Hq, shp.T, shp.d, shp.seed).to(dev)
+        o, lse = attn.fwd(q, k, v, causal=shp.causal, scale=shp.scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def run():
+            attn.bwd(q, k, v, o, lse, do, causal=shp.causal, scale=shp.scale, dq=dq, dk=dk, dv=dv)
+        work, unit = 2.5 * shp.flops() / 1e12, "TFLOP/s (5-GEMM algorithmic)"
     elif args.op in ("decode", "decode_fp8"):
         shp = W.DECODE_LLAMA
         q, kc, vc, sl = W.decode_inputs(shp)
