@@ -34,6 +34,7 @@ from .attention import (  # noqa: F401
     decode_split_merge,
     count_blocks,
     attention_backward,
+    attention_backward_rows,
 )
 from .rmsnorm import rmsnorm, rmsnorm_rows, rmsnorm_residual  # noqa: F401
 from .fp8 import (  # noqa: F401

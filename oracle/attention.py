@@ -365,3 +365,41 @@ def attention_backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarra
             dq[b, h] = (ds @ kk) * scale
             dk[b, h // g] += (ds.T @ q[b, h]) * scale
     return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, do, causal: bool, scale: float, b: int, kvh: int, q_rows, k_rows):
+    """The gradients of ``attention_backward`` on selected rows of one K/V group, for sizes
+    where the full gradients are too large: dQ on rows ``q_rows`` of each of the g query heads
+    that read K/V head (b, kvh), and dK, dV on rows ``k_rows`` of that head. Each head's O, L
+    and D_i = dO_i . O_i come from the full forward of that head (every query row).
+    Returns dQ [g, len(q_rows), d], dK and dV [len(k_rows), d].
+    """
+    Hq, Tq = q.shape[1], q.shape[2]
+    Hkv, Tk = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    k_rows = np.asarray(k_rows, dtype=np.int64)
+    kk, vv = k[b, kvh], v[b, kvh]
+    dq = np.zeros((g, len(q_rows), q.shape[3]))
+    dk = np.zeros((len(k_rows), k.shape[3]))
+    dv = np.zeros((len(k_rows), v.shape[3]))
+    all_rows = np.arange(Tq)
+    for gi in range(g):
+        h = kvh * g + gi
+        o, lse = attention_rows(q[b:b + 1, h:h + 1], k[b:b + 1, kvh:kvh + 1], v[b:b + 1, kvh:kvh + 1], 0, 0,
+                                all_rows, causal, scale)
+        D = np.sum(do[b, h] * o, axis=1)
+        # dQ rows: full key range of each selected query row
+        vis = _visible_mask(q_rows, Tk, causal)
+        s = np.where(vis, (q[b, h, q_rows] @ kk.T) * scale, NEG_INF)
+        p = np.exp(s - lse[q_rows][:, None])
+        ds = p * (do[b, h, q_rows] @ vv.T - D[q_rows][:, None])
+        dq[gi] = (ds @ kk) * scale
+        # dK, dV rows: every query row against the selected keys
+        visk = _visible_mask(all_rows, Tk, causal)[:, k_rows]
+        sk = np.where(visk, (q[b, h] @ kk[k_rows].T) * scale, NEG_INF)
+        pk = np.exp(sk - lse[:, None])
+        dv += pk.T @ do[b, h]
+        dsk = pk * (do[b, h] @ vv[k_rows].T - D[:, None])
+        dk += (dsk.T @ q[b, h]) * scale
+    return dq, dk, dv

@@ -67,6 +67,31 @@ def test_prefill_full_size_sampled(attn, shape):
     _check_sampled(q, k, v, o, lse, shape.causal, shape.scale, sorted(pairs), shape.seed)
 
 
+@pytest.mark.parametrize("shape,group", [(W.GQA_LLAMA, (1, 5)), (W.GQA_QWEN, (0, 3))], ids=["gqa-llama", "gqa-qwen"])
+def test_backward_full_size_sampled(attn, shape, group):
+    # the full backward on the workload; the oracle checks sampled dQ rows of every query head of
+    # one K/V group and sampled dK, dV rows of that K/V head (tolerance as tests/test_gpu_backward.py)
+    q, k, v = W.attention_inputs(shape)[:3]
+    do = W.grad_output(shape.B, shape.Hq, shape.T, shape.d, shape.seed)
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
+    o, lse = attn.fwd(qd, kd, vd, causal=shape.causal, scale=shape.scale)
+    dq, dk, dv = attn.bwd(qd, kd, vd, o, lse, dod, causal=shape.causal, scale=shape.scale)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    b, kvh = group
+    g = shape.Hq // shape.Hkv
+    rows = _sample_rows(shape.T, shape.seed + 77, n_random=12)
+    sl = slice(b, b + 1)
+    rq, rk, rv = oracle.attention_backward_rows(f64(q[sl]), f64(k[sl]), f64(v[sl]), f64(do[sl]), shape.causal,
+                                                shape.scale, 0, kvh, rows, rows)
+    got_q = f64(dq[b, kvh * g:(kvh + 1) * g][:, rows])
+    for name, got, want in (("dQ", got_q, rq), ("dK", f64(dk[b, kvh, rows]), rk), ("dV", f64(dv[b, kvh, rows]), rv)):
+        err = np.abs(got - want)
+        assert np.all(np.isfinite(got)), name
+        assert err.max() <= 2e-2 * np.abs(want).max() + 1e-6, (name, err.max(), np.abs(want).max())
+        assert err.mean() <= 1e-2 * np.abs(want).mean() + 1e-7, (name, err.mean(), np.abs(want).mean())
+
+
 def test_decode_full_size(attn):
     shp = W.DECODE_LLAMA
     q, kc, vc, sl = W.decode_inputs(shp)

@@ -98,3 +98,17 @@ def test_backward_closed_forms():
     dq, dk, dv = _oracle_grads(q1, k1, v1, do1, False, scale)
     assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
     assert np.allclose(dv[0, 0, 0], do1[0].sum(axis=(0, 1)), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_match_the_full_gradients(causal):
+    # the sampled-row form used at full sizes against the pinned full gradients
+    q, k, v, do = _inputs(2, 6, 2, 50, 50, 8, seed=13)
+    scale = 0.4
+    dq, dk, dv = _oracle_grads(q, k, v, do, causal, scale)
+    qr, kr = [0, 7, 31, 49], [0, 1, 25, 49]
+    for b, kvh in ((0, 0), (1, 1)):
+        rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, causal, scale, b, kvh, qr, kr)
+        for gi in range(3):
+            assert np.allclose(rq[gi], dq[b, kvh * 3 + gi, qr], atol=1e-12)
+        assert np.allclose(rk, dk[b, kvh, kr], atol=1e-12) and np.allclose(rv, dv[b, kvh, kr], atol=1e-12)
