@@ -13,7 +13,7 @@
 // Kernel 1 (split): one CTA per (split, K/V head, block of <= 4 query heads of
 // its group, sequence). One producer thread streams the split's K and V rows
 // into a ring of shared-memory stages with bulk asynchronous copies (each stage
-// = 32 contiguous rows, completing on an mbarrier); four consumer warps read
+// = 64 contiguous rows, completing on an mbarrier); four consumer warps read
 // the stages with 16-byte shared loads (d/8 lanes per row, packed fp32x2 FMAs,
 // a shuffle reduction per head), keep a running (m, l, o) per query
 // head in registers, merge them at the end and write one fp32 partial per
@@ -43,8 +43,8 @@ struct DecodeCfg {
   static constexpr int kElems = 8 * kChunks;           // row elements per lane
   static constexpr int kTokPerPass = 32 / kLanesPerTok;
   static constexpr int kConsumerWarps = 4;
-  static constexpr int kTile = 32;                     // rows (tokens) per stage
-  static constexpr int kStages = 4;
+  static constexpr int kTile = 64;                     // rows (tokens) per stage: R = 8 rows per lane
+  static constexpr int kStages = 2;                    // group (d = 128) per tile; 3 CTAs per SM
   static constexpr int kTokPerWarp = kTile / kConsumerWarps;
   static constexpr int kPasses = kTokPerWarp / kTokPerPass;
   static constexpr int kRowBytes = D * EB;
@@ -109,8 +109,10 @@ __device__ __forceinline__ void load_row_chunks(const uint8_t* row, int sub, flo
   }
 }
 
+// 3 CTAs per SM (registers capped at 136; the widest instances spill ~70 bytes, which costs less
+// than the latency hiding of a third CTA gains)
 template <int D, int G, int EB>
-__global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads, 3)
     decode_split_kernel(const DecodeParams p) {
   using Cfg = DecodeCfg<D, EB>;
   constexpr int E = Cfg::kElems;
