@@ -13,17 +13,19 @@
 //   bwd_delta_kernel   D_i = dO_i . O_i, one warp per row (HBM-bound, fp32 into the workspace).
 //   bwd_dkdv_kernel    one CTA per (block of 128 keys, K/V head): walks the g query heads x
 //                      the visible query blocks; per block S^T = K Q^T and dP^T = V dO^T into
-//                      TMEM, 8 warps (two per key row) form P^T and dS^T (bf16) inside those
-//                      TMEM tiles, then dV += P^T dO and dK += dS^T Q with the
-//                      A operand from TMEM; dV and dK stay in TMEM until the end.
+//                      TMEM, 8 warps (two per key row) form P^T (phase 1, from S^T alone) and
+//                      dS^T (phase 2, with dP^T) as bf16 pairs inside S^T's columns, then
+//                      dV += P^T dO and dK += dS^T Q with the A operand from TMEM; dV and dK
+//                      stay in TMEM until the end.
 //   bwd_dq_kernel      one CTA per (block of 128 queries, query head): walks the visible key
-//                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into TMEM, dQ += dS K.
+//                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into S's columns, dQ += dS K.
 // Each kernel: warps 0-7 compute (warps w and w + 4 share TMEM lanes 32(w mod 4) .. + 31 and
 // take one half of the row's 128 columns each), warp 8 issues the TMA copies (two stages of the
-// walked operand pair), warp 9 issues the MMAs from one thread. Every
-// handoff is an mbarrier with a bounded wait; the steps of one block run one after the
-// other (recomputing S and dP in the dQ kernel costs 2 of its 3 GEMMs; the layout keeps
-// every output with one owner).
+// walked operand pair), warp 9 issues the MMAs from one thread. Every handoff is an mbarrier
+// with a bounded wait. The two 128-column score regions swap roles every block, so the next
+// block's scores go into the region phase 2 has just consumed while this block's gradient
+// GEMMs run, and phase 1 of the next block overlaps them (recomputing S and dP in the dQ
+// kernel costs 2 of its 3 GEMMs; the layout keeps every output with one owner).
 //
 // P is rounded to bf16 for dV = P^T dO and dS to bf16 for the two gradient GEMMs; all
 // accumulation is fp32 in TMEM; outputs are rounded once to bf16.
@@ -47,8 +49,9 @@ struct BwdCfg {
   static constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false);
   // [128 x D] += A (TMEM, 128 x 128 bf16) . B (128 x D, MN-major)
   static constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, D, true);
-  // TMEM columns: the two 128x128 fp32 score tiles, then the fp32 accumulators
-  static constexpr uint32_t kTmS = 0, kTmDP = 128, kTmAcc0 = 256, kTmAcc1 = 256 + D;
+  // TMEM columns: two 128-column score regions [0, 128) and [128, 256) that swap roles every block,
+  // then the fp32 accumulators (dV and dK, or dQ)
+  static constexpr uint32_t kTmAcc0 = 256, kTmAcc1 = 256 + D;
 };
 
 struct BwdParams {
@@ -74,16 +77,17 @@ __device__ __forceinline__ void bwd_mma_scores(uint32_t d_tmem, uint32_t a_smem,
   }
 }
 
-// D[128 x D] (+)= A (TMEM: 128 rows x 128 bf16) . B (128 rows x D, MN-major). A's bf16 pairs sit
-// in two ranges of the 128-column tile they replaced: columns 0..63 of the tile at [0, 32),
-// columns 64..127 at [64, 96) (each half of the compute warps writes inside the columns it read).
+// D[128 x D] (+)= A (TMEM, 128 rows x 128 bf16) . B (128 rows x D, MN-major), with A's bf16 pairs
+// in the layout the score region holds after the two compute phases: for each half h of the 128
+// columns, 32 columns at region + 64 h + a_off (a_off 0: P^T, 32: dS^T).
 template <int D>
-__device__ __forceinline__ void bwd_mma_accumulate(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
+__device__ __forceinline__ void bwd_mma_accumulate_split(uint32_t d_tmem, uint32_t region, uint32_t a_off,
+                                                         uint32_t b_smem, bool accumulate) {
   using Cfg = BwdCfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < 128 / 16; ++kk)  // 16 rows of B = 2048 bytes per step
-    umma_ts(d_tmem, a_tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024),
-            Cfg::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 128 / 16; ++kk)
+    umma_ts(d_tmem, region + (kk >> 2) * 64 + a_off + (kk & 3) * 8,
+            make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024), Cfg::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Half `half` (columns [half*D/2, (half+1)*D/2)) of one row (this thread's TMEM lane) of a
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::kTileBytes;
   // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
-  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, p_ready, acc_done;
+  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, p_ready, acc_done;
   __shared__ __align__(16) float lse_s[128];  // read as float4
   __shared__ __align__(16) float dl_s[128];
   __shared__ uint32_t tmem_holder;
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_ready, 1);
+    mbar_init(&dp_ready, 1);
     mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
@@ -229,22 +234,40 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
+      // The two 128-column score regions swap roles every block: S^T(i) goes to region i & 1 and
+      // dP^T(i) to the other one. The compute warps turn S^T(i) into P^T(i) (phase 1, needs only
+      // S^T) and then, with dP^T(i), into dS^T(i) (phase 2), both kept inside S^T(i)'s region, so
+      // dP^T(i)'s region is free once phase 2 is done: S^T(i + 1) goes there while dV(i), dK(i)
+      // read P^T(i), dS^T(i), and dP^T(i + 1) follows into S^T(i)'s region (the tensor pipe runs
+      // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dV(i), dK(i), dP^T(i + 1).
       bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      auto aQ_of = [&](int it) { return smem_u32(smem + (2 + 2 * (it & 1)) * Cfg::kTileBytes); };
+      auto aDO_of = [&](int it) { return smem_u32(smem + (3 + 2 * (it & 1)) * Cfg::kTileBytes); };
+      if (ok && n_it > 0) {
+        ok = mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
+        if (ok) {
+          tc_fence_after();
+          bwd_mma_scores<D>(tmem, aK, aQ_of(0));  // S^T(0) = K Q^T into region 0
+          umma_commit(&s_ready);
+        }
+      }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it & 1;
-        const uint32_t aQ = smem_u32(smem + (2 + 2 * s) * Cfg::kTileBytes);
-        const uint32_t aDO = smem_u32(smem + (3 + 2 * s) * Cfg::kTileBytes);
-        if (!mbar_wait(&full[s], static_cast<uint32_t>(it >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
-        tc_fence_after();
-        bwd_mma_scores<D>(tmem + Cfg::kTmS, aK, aQ);    // S^T = K Q^T
-        bwd_mma_scores<D>(tmem + Cfg::kTmDP, aV, aDO);  // dP^T = V dO^T
-        umma_commit(&s_ready);
+        const uint32_t r_s = tmem + (it & 1) * 128, r_d = tmem + ((it + 1) & 1) * 128;
+        bwd_mma_scores<D>(r_d, aV, aDO_of(it));  // dP^T(i) = V dO^T
+        umma_commit(&dp_ready);
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
-        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc0, tmem + Cfg::kTmS, aDO, it > 0);   // dV += P^T dO
-        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc1, tmem + Cfg::kTmDP, aQ, it > 0);   // dK += dS^T Q
-        umma_commit(&empty[s]);
+        if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
+          if (!mbar_wait(&full[(it + 1) & 1], static_cast<uint32_t>((it + 1) >> 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+            break;
+          tc_fence_after();
+          bwd_mma_scores<D>(r_d, aK, aQ_of(it + 1));
+          umma_commit(&s_ready);
+        }
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aDO_of(it), it > 0);   // dV += P^T dO
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, aQ_of(it), it > 0);   // dK += dS^T Q
+        umma_commit(&empty[it & 1]);
       }
       umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
     }
@@ -269,41 +292,61 @@ __global__ void __launch_bounds__(320, 1)
         else dl_s[row] = q < p.Tq ? p.delta[r] : 0.f;
       }
       named_bar_sync(1, 256);
+      const uint32_t r_s = tmem + lane_off + (it & 1) * 128, r_d = tmem + lane_off + ((it + 1) & 1) * 128;
+      float pv[64];  // this thread's 64 probabilities, kept between the two phases
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(it) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
-        // This half's 64 queries in two chunks of 32; chunk cc reads columns [q0, q0 + 32) and
-        // writes its bf16 pairs to [q0 / 2 + half * 32, + 16), inside the columns this half read
-        // and already consumed.
+        // phase 1: P^T from S^T alone. This half's 64 queries in two chunks of 32; chunk cc reads
+        // columns [64 half + 32 cc, + 32) and writes its bf16 pairs to [64 half + 16 cc, + 16),
+        // inside what this half has read
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int q0 = half * 64 + cc * 32;
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + Cfg::kTmS + q0, sr);
-          tmem_ld32(tmem + lane_off + Cfg::kTmDP + q0, dr);
-          uint32_t pp[16], dd[16];
+          uint32_t sr[32];
+          tmem_ld32(r_s + q0, sr);
+          uint32_t pp[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + 4 * v4);
-            const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + 4 * v4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], gv[4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int qi = q0 + 4 * v4 + e;
               const bool vis = key_ok && (!p.causal || key <= i0 + qi);
-              pv[e] = vis ? ex2_approx(__uint_as_float(sr[4 * v4 + e]) * c - lv[e]) : 0.f;
-              gv[e] = pv[e] * (__uint_as_float(dr[4 * v4 + e]) - dvv[e]);
+              pv[cc * 32 + 4 * v4 + e] = vis ? ex2_approx(__uint_as_float(sr[4 * v4 + e]) * c - lv[e]) : 0.f;
             }
-            pp[2 * v4] = pack_bf16x2(pv[0], pv[1]);
-            pp[2 * v4 + 1] = pack_bf16x2(pv[2], pv[3]);
+            pp[2 * v4] = pack_bf16x2(pv[cc * 32 + 4 * v4], pv[cc * 32 + 4 * v4 + 1]);
+            pp[2 * v4 + 1] = pack_bf16x2(pv[cc * 32 + 4 * v4 + 2], pv[cc * 32 + 4 * v4 + 3]);
+          }
+          tmem_st16(r_s + half * 64 + cc * 16, pp);
+        }
+      }
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&dp_ready, static_cast<uint32_t>(it) & 1u, abort_p,
+                                                      kBwdWaitTimeoutNs));
+      if (ok) {
+        tc_fence_after();
+        // phase 2: dS^T = P^T (dP^T - D) into [64 half + 32 + 16 cc, + 16) of S^T's region (S^T
+        // values there were consumed in phase 1); dP^T's region is then free
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int q0 = half * 64 + cc * 32;
+          uint32_t dr[32];
+          tmem_ld32(r_d + q0, dr);
+          uint32_t dd[16];
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + 4 * v4);
+            const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float gv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              gv[e] = pv[cc * 32 + 4 * v4 + e] * (__uint_as_float(dr[4 * v4 + e]) - dvv[e]);
             dd[2 * v4] = pack_bf16x2(gv[0], gv[1]);
             dd[2 * v4 + 1] = pack_bf16x2(gv[2], gv[3]);
           }
-          const uint32_t out_col = half * 64 + cc * 16;
-          tmem_st16(tmem + lane_off + Cfg::kTmS + out_col, pp);
-          tmem_st16(tmem + lane_off + Cfg::kTmDP + out_col, dd);
+          tmem_st16(r_s + half * 64 + 32 + cc * 16, dd);
         }
         tmem_st_wait();
       }
@@ -341,7 +384,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + Cfg::kTileBytes;
   // stage s: K at 2 + 2s, V at 3 + 2s (in tiles)
-  __shared__ uint64_t qd_full, full[2], empty[2], s_ready, p_ready, acc_done;
+  __shared__ uint64_t qd_full, full[2], empty[2], s_ready, dp_ready, p_ready, acc_done;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
 
@@ -360,6 +403,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(&s_ready, 1);
+    mbar_init(&dp_ready, 1);
     mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
@@ -409,21 +453,35 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
+      // Regions swap roles as in the dK/dV kernel: S(j) in region j & 1, dP(j) in the other; dS(j)
+      // is written inside S(j)'s region, so S(j + 1) can go into dP(j)'s region while dQ(j) runs.
       bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
+      auto aK_of = [&](int j) { return smem_u32(smem + (2 + 2 * (j & 1)) * Cfg::kTileBytes); };
+      auto aV_of = [&](int j) { return smem_u32(smem + (3 + 2 * (j & 1)) * Cfg::kTileBytes); };
+      if (ok && n_j > 0) {
+        ok = mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
+        if (ok) {
+          tc_fence_after();
+          bwd_mma_scores<D>(tmem, aQ, aK_of(0));  // S(0) = Q K^T into region 0
+          umma_commit(&s_ready);
+        }
+      }
       for (int j = 0; ok && j < n_j; ++j) {
-        const int s = j & 1;
-        const uint32_t aK = smem_u32(smem + (2 + 2 * s) * Cfg::kTileBytes);
-        const uint32_t aV = smem_u32(smem + (3 + 2 * s) * Cfg::kTileBytes);
-        if (!mbar_wait(&full[s], static_cast<uint32_t>(j >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
-        tc_fence_after();
-        bwd_mma_scores<D>(tmem + Cfg::kTmS, aQ, aK);    // S = Q K^T
-        bwd_mma_scores<D>(tmem + Cfg::kTmDP, aDO, aV);  // dP = dO V^T
-        umma_commit(&s_ready);
+        const uint32_t r_s = tmem + (j & 1) * 128, r_d = tmem + ((j + 1) & 1) * 128;
+        bwd_mma_scores<D>(r_d, aDO, aV_of(j));  // dP(j) = dO V^T
+        umma_commit(&dp_ready);
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(j) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
-        bwd_mma_accumulate<D>(tmem + Cfg::kTmAcc0, tmem + Cfg::kTmDP, aK, j > 0);  // dQ += dS K
-        umma_commit(&empty[s]);
+        if (j + 1 < n_j) {
+          if (!mbar_wait(&full[(j + 1) & 1], static_cast<uint32_t>((j + 1) >> 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+            break;
+          tc_fence_after();
+          bwd_mma_scores<D>(r_d, aQ, aK_of(j + 1));
+          umma_commit(&s_ready);
+        }
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aK_of(j), j > 0);  // dQ += dS K
+        umma_commit(&empty[j & 1]);
       }
       umma_commit(&acc_done);
     }
@@ -441,31 +499,42 @@ __global__ void __launch_bounds__(320, 1)
     const float c = p.c;
     bool ok = true;
     for (int j = 0; j < n_j; ++j) {
+      const uint32_t r_s = tmem + lane_off + (j & 1) * 128, r_d = tmem + lane_off + ((j + 1) & 1) * 128;
+      float pv[64];  // this thread's 64 probabilities, kept between the two phases
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(j) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
-        // this half's 64 keys in two chunks of 32; dS pairs go inside the columns this half read
+        // phase 1: P from S alone (this half's 64 keys in two chunks of 32)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int k0 = half * 64 + cc * 32;
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + Cfg::kTmS + k0, sr);
-          tmem_ld32(tmem + lane_off + Cfg::kTmDP + k0, dr);
+          uint32_t sr[32];
+          tmem_ld32(r_s + k0, sr);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int key = j * 128 + k0 + k;
+            const bool vis = key < p.Tk && (!p.causal || key <= q);
+            pv[cc * 32 + k] = vis ? ex2_approx(__uint_as_float(sr[k]) * c - lse2) : 0.f;
+          }
+        }
+      }
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&dp_ready, static_cast<uint32_t>(j) & 1u, abort_p,
+                                                      kBwdWaitTimeoutNs));
+      if (ok) {
+        tc_fence_after();
+        // phase 2: dS = P (dP - D) as bf16 pairs into [64 half + 16 cc, + 16) of S's region
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int k0 = half * 64 + cc * 32;
+          uint32_t dr[32];
+          tmem_ld32(r_d + k0, dr);
           uint32_t dd[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float dv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = j * 128 + k0 + 2 * k + e;
-              const bool vis = key < p.Tk && (!p.causal || key <= q);
-              const float pv = vis ? ex2_approx(__uint_as_float(sr[2 * k + e]) * c - lse2) : 0.f;
-              dv[e] = pv * (__uint_as_float(dr[2 * k + e]) - dl);
-            }
-            dd[k] = pack_bf16x2(dv[0], dv[1]);
-          }
-          tmem_st16(tmem + lane_off + Cfg::kTmDP + half * 64 + cc * 16, dd);  // dS
+          for (int k = 0; k < 16; ++k)
+            dd[k] = pack_bf16x2(pv[cc * 32 + 2 * k] * (__uint_as_float(dr[2 * k]) - dl),
+                                pv[cc * 32 + 2 * k + 1] * (__uint_as_float(dr[2 * k + 1]) - dl));
+          tmem_st16(r_s + half * 64 + cc * 16, dd);
         }
         tmem_st_wait();
       }
