@@ -134,6 +134,34 @@ def test_decode_fp8_needs_scales(lib):
     assert lib.attn_decode_fp8(*args) == 3
 
 
+def _bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, Hq=4, Hkv=2,
+             Tq=300, Tk=300, d=128, causal=1, scale=0.1, ws=FAKE, wsb=None, stream=None)
+    a.update(kw)
+    if a["wsb"] is None:
+        a["wsb"] = lib.attn_bwd_workspace_size(a["B"], a["Hq"], a["Tq"])
+    return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["B"],
+                        a["Hq"], a["Hkv"], a["Tq"], a["Tk"], a["d"], a["causal"], a["scale"], a["ws"], a["wsb"],
+                        a["stream"])
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.attn_bwd_workspace_size(2, 32, 8192) == 2 * 32 * 8192 * 4
+    assert lib.attn_bwd_workspace_size(1, 1, 3) == 256  # rounded up to 256 bytes
+    assert lib.attn_bwd_workspace_size(0, 1, 3) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(do=None), 1), (dict(dv=None), 1), (dict(Hq=6, Hkv=4), 1),
+    (dict(Tk=0), 1), (dict(scale=0.0), 1), (dict(causal=2), 1), (dict(d=96), 2), (dict(dk=FAKE + 8), 3),
+    (dict(lse=FAKE + 2), 3), (dict(ws=None), 4), (dict(wsb=16), 4), (dict(ws=FAKE + 8), 3),
+])
+def test_bwd_rejects_invalid_arguments(lib, kw, code):
+    n0 = lib.attn_kernel_launches()
+    assert _bwd(lib, **kw) == code
+    assert lib.attn_kernel_launches() == n0
+
+
 def test_selftest_rejects_out_of_range_bound(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == 1
     assert lib.attn_selftest_wait_timeout(2_000_000, None) == 1
