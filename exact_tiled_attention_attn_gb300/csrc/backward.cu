@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::kTileBytes;
   // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
-  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, p_ready, acc_done;
+  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, p1_ready, p_ready, acc_done;
   __shared__ __align__(16) float lse_s[128];  // read as float4
   __shared__ __align__(16) float dl_s[128];
   __shared__ uint32_t tmem_holder;
@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&s_ready, 1);
     mbar_init(&dp_ready, 1);
+    mbar_init(&p1_ready, 8);
     mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
@@ -239,7 +240,8 @@ __global__ void __launch_bounds__(320, 1)
       // S^T) and then, with dP^T(i), into dS^T(i) (phase 2), both kept inside S^T(i)'s region, so
       // dP^T(i)'s region is free once phase 2 is done: S^T(i + 1) goes there while dV(i), dK(i)
       // read P^T(i), dS^T(i), and dP^T(i + 1) follows into S^T(i)'s region (the tensor pipe runs
-      // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dV(i), dK(i), dP^T(i + 1).
+      // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
+      // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
       bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       auto aQ_of = [&](int it) { return smem_u32(smem + (2 + 2 * (it & 1)) * Cfg::kTileBytes); };
@@ -256,6 +258,10 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t r_s = tmem + (it & 1) * 128, r_d = tmem + ((it + 1) & 1) * 128;
         bwd_mma_scores<D>(r_d, aV, aDO_of(it));  // dP^T(i) = V dO^T
         umma_commit(&dp_ready);
+        // dV needs only P^T: it runs while phase 2 forms dS^T in the other columns of the region
+        if (!mbar_wait(&p1_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+        tc_fence_after();
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aDO_of(it), it > 0);   // dV += P^T dO
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
         if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
@@ -265,7 +271,6 @@ __global__ void __launch_bounds__(320, 1)
           bwd_mma_scores<D>(r_d, aK, aQ_of(it + 1));
           umma_commit(&s_ready);
         }
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aDO_of(it), it > 0);   // dV += P^T dO
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, aQ_of(it), it > 0);   // dK += dS^T Q
         umma_commit(&empty[it & 1]);
       }
@@ -322,7 +327,11 @@ __global__ void __launch_bounds__(320, 1)
           }
           tmem_st16(r_s + half * 64 + cc * 16, pp);
         }
+        tmem_st_wait();
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p1_ready);  // P^T(i) is in TMEM (every block, also after a failed wait)
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&dp_ready, static_cast<uint32_t>(it) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
