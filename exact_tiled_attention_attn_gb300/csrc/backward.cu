@@ -49,9 +49,13 @@ struct BwdCfg {
   static constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false);
   // [128 x D] += A (TMEM, 128 x 128 bf16) . B (128 x D, MN-major)
   static constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, D, true);
-  // TMEM columns: two 128-column score regions [0, 128) and [128, 256) that swap roles every block,
-  // then the fp32 accumulators (dV and dK, or dQ)
+  // dK/dV kernel TMEM columns: two 128-column score regions [0, 128) and [128, 256) that swap roles
+  // every block, then the fp32 accumulators dV and dK
   static constexpr uint32_t kTmAcc0 = 256, kTmAcc1 = 256 + D;
+  // dQ kernel: Q and dO resident, three K stages and two V stages (7 tiles); TMEM: S in [0, 128) and
+  // [128, 256) by turns, dP in [256, 384), the fp32 dQ accumulator from 384
+  static constexpr int kSmemBytesDq = (7 * kTileBytes + 1024) > 116 * 1024 ? (7 * kTileBytes + 1024) : 116 * 1024;
+  static constexpr uint32_t kTmDp = 256, kTmDq = 384;
 };
 
 struct BwdParams {
@@ -161,8 +165,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sV = smem + Cfg::kTileBytes;
   // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
   __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, p1_ready, p_ready, acc_done;
-  __shared__ __align__(16) float lse_s[128];  // read as float4
-  __shared__ __align__(16) float dl_s[128];
+  __shared__ __align__(16) float nl_s[128];   // -L log2(e) per query row, read as float4
+  __shared__ __align__(16) float ndl_s[128];  // -D per query row
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
 
@@ -284,17 +288,19 @@ __global__ void __launch_bounds__(320, 1)
     const int key = j0 + row;
     const bool key_ok = key < p.Tk;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float c = p.c;
+    const float2 c2 = make_float2(p.c, p.c);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = kvh * p.g + it / n_i;
       const int i0 = (i_first + it % n_i) * 128;
-      named_bar_sync(1, 256);  // the previous block's readers of lse_s / dl_s are done
+      // every key of the block is visible to every query of the query block: no mask
+      const bool full = j0 + 128 <= p.Tk && (!p.causal || j0 + 127 <= i0);
+      named_bar_sync(1, 256);  // the previous block's readers of nl_s / ndl_s are done
       {
         const int q = i0 + row;
         const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + q;
-        if (half == 0) lse_s[row] = q < p.Tq ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
-        else dl_s[row] = q < p.Tq ? p.delta[r] : 0.f;
+        if (half == 0) nl_s[row] = q < p.Tq ? -(p.lse[r] * kLog2e) : -INFINITY;  // rows past Tq: P = 0
+        else ndl_s[row] = q < p.Tq ? -p.delta[r] : 0.f;
       }
       named_bar_sync(1, 256);
       const uint32_t r_s = tmem + lane_off + (it & 1) * 128, r_d = tmem + lane_off + ((it + 1) & 1) * 128;
@@ -311,20 +317,26 @@ __global__ void __launch_bounds__(320, 1)
           const int q0 = half * 64 + cc * 32;
           uint32_t sr[32];
           tmem_ld32(r_s + q0, sr);
-          uint32_t pp[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + 4 * v4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int qi = q0 + 4 * v4 + e;
-              const bool vis = key_ok && (!p.causal || key <= i0 + qi);
-              pv[cc * 32 + 4 * v4 + e] = vis ? ex2_approx(__uint_as_float(sr[4 * v4 + e]) * c - lv[e]) : 0.f;
-            }
-            pp[2 * v4] = pack_bf16x2(pv[cc * 32 + 4 * v4], pv[cc * 32 + 4 * v4 + 1]);
-            pp[2 * v4 + 1] = pack_bf16x2(pv[cc * 32 + 4 * v4 + 2], pv[cc * 32 + 4 * v4 + 3]);
+            const float4 l4 = *reinterpret_cast<const float4*>(nl_s + q0 + 4 * v4);
+            const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * v4]), __uint_as_float(sr[4 * v4 + 1])), c2,
+                                          make_float2(l4.x, l4.y));
+            const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(sr[4 * v4 + 2]), __uint_as_float(sr[4 * v4 + 3])),
+                                          c2, make_float2(l4.z, l4.w));
+            pv[cc * 32 + 4 * v4] = ex2_approx(x01.x);
+            pv[cc * 32 + 4 * v4 + 1] = ex2_approx(x01.y);
+            pv[cc * 32 + 4 * v4 + 2] = ex2_approx(x23.x);
+            pv[cc * 32 + 4 * v4 + 3] = ex2_approx(x23.y);
           }
+          if (!full) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (!(key_ok && (!p.causal || key <= i0 + q0 + k))) pv[cc * 32 + k] = 0.f;
+          }
+          uint32_t pp[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pp[k] = pack_bf16x2(pv[cc * 32 + 2 * k], pv[cc * 32 + 2 * k + 1]);
           tmem_st16(r_s + half * 64 + cc * 16, pp);
         }
         tmem_st_wait();
@@ -346,14 +358,15 @@ __global__ void __launch_bounds__(320, 1)
           uint32_t dd[16];
 #pragma unroll
           for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + 4 * v4);
-            const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float gv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              gv[e] = pv[cc * 32 + 4 * v4 + e] * (__uint_as_float(dr[4 * v4 + e]) - dvv[e]);
-            dd[2 * v4] = pack_bf16x2(gv[0], gv[1]);
-            dd[2 * v4 + 1] = pack_bf16x2(gv[2], gv[3]);
+            const float4 d4 = *reinterpret_cast<const float4*>(ndl_s + q0 + 4 * v4);
+            const float2 g01 = __fmul2_rn(make_float2(pv[cc * 32 + 4 * v4], pv[cc * 32 + 4 * v4 + 1]),
+                                          __fadd2_rn(make_float2(__uint_as_float(dr[4 * v4]), __uint_as_float(dr[4 * v4 + 1])),
+                                                     make_float2(d4.x, d4.y)));
+            const float2 g23 = __fmul2_rn(make_float2(pv[cc * 32 + 4 * v4 + 2], pv[cc * 32 + 4 * v4 + 3]),
+                                          __fadd2_rn(make_float2(__uint_as_float(dr[4 * v4 + 2]), __uint_as_float(dr[4 * v4 + 3])),
+                                                     make_float2(d4.z, d4.w)));
+            dd[2 * v4] = pack_bf16x2(g01.x, g01.y);
+            dd[2 * v4 + 1] = pack_bf16x2(g23.x, g23.y);
           }
           tmem_st16(r_s + half * 64 + 32 + cc * 16, dd);
         }
@@ -392,8 +405,10 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + Cfg::kTileBytes;
-  // stage s: K at 2 + 2s, V at 3 + 2s (in tiles)
-  __shared__ uint64_t qd_full, full[2], empty[2], s_ready, dp_ready, p_ready, acc_done;
+  // K(j) in tile 2 + j mod 3, V(j) in tile 5 + j mod 2. K is read by S(j) and, one block later, by
+  // dQ(j), while S(j + 2) is already wanted: three K tiles are live at once.
+  __shared__ uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_ready[2], dp_ready, p_ready,
+      acc_done;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
 
@@ -407,11 +422,15 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&qd_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    mbar_init(&s_ready, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&s_ready[s], 1);
+    }
     mbar_init(&dp_ready, 1);
     mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
@@ -429,7 +448,7 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_p = &abort_flag;
 
   if (warp == 8) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: K(j) then V(j), each on its own ring ----------------
     if (lane == 0 && n_j > 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
@@ -441,16 +460,19 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sDO + kb * Cfg::kBoxBytes, &tmDO, &qd_full, kb * 64, i0, b * p.Hq + h);
       }
       for (int j = 0; j < n_j; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&empty[s], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+        const int sk = j % 3, sv = j & 1;
+        if (j >= 3 && !mbar_wait(&k_empty[sk], static_cast<uint32_t>(j / 3 - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
           break;
-        uint8_t* sK = smem + (2 + 2 * s) * Cfg::kTileBytes;
-        uint8_t* sV = smem + (3 + 2 * s) * Cfg::kTileBytes;
-        mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
-        for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
-          tma_load_3d(sK + kb * Cfg::kBoxBytes, &tmK, &full[s], kb * 64, j * 128, b * p.Hkv + kvh);
-          tma_load_3d(sV + kb * Cfg::kBoxBytes, &tmV, &full[s], kb * 64, j * 128, b * p.Hkv + kvh);
-        }
+        uint8_t* sK = smem + (2 + sk) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&k_full[sk], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sK + kb * Cfg::kBoxBytes, &tmK, &k_full[sk], kb * 64, j * 128, b * p.Hkv + kvh);
+        if (j >= 2 && !mbar_wait(&v_empty[sv], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+          break;
+        uint8_t* sV = smem + (5 + sv) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&v_full[sv], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sV + kb * Cfg::kBoxBytes, &tmV, &v_full[sv], kb * 64, j * 128, b * p.Hkv + kvh);
       }
       if (*abort_p) {
         const uint64_t t0 = global_timer_ns();
@@ -462,35 +484,37 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      // Regions swap roles as in the dK/dV kernel: S(j) in region j & 1, dP(j) in the other; dS(j)
-      // is written inside S(j)'s region, so S(j + 1) can go into dP(j)'s region while dQ(j) runs.
+      // S(j) goes to region j & 1 and dP(j) always to [256, 384); phase 2 writes dS(j) inside S(j)'s
+      // region. Once phase 2 of block j is done: dP(j + 1) (phase 2 of block j + 1 waits for it
+      // first), dQ(j) += dS(j) K(j), and S(j + 2) into S(j)'s region after dQ(j) has read it (the
+      // tensor pipe runs one thread's MMAs in issue order). S(j + 1) was issued a block earlier, so
+      // phase 1 of block j + 1 starts at once and the tensor pipe has work during phase 2.
       bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      auto aK_of = [&](int j) { return smem_u32(smem + (2 + 2 * (j & 1)) * Cfg::kTileBytes); };
-      auto aV_of = [&](int j) { return smem_u32(smem + (3 + 2 * (j & 1)) * Cfg::kTileBytes); };
-      if (ok && n_j > 0) {
-        ok = mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
-        if (ok) {
-          tc_fence_after();
-          bwd_mma_scores<D>(tmem, aQ, aK_of(0));  // S(0) = Q K^T into region 0
-          umma_commit(&s_ready);
-        }
-      }
-      for (int j = 0; ok && j < n_j; ++j) {
-        const uint32_t r_s = tmem + (j & 1) * 128, r_d = tmem + ((j + 1) & 1) * 128;
-        bwd_mma_scores<D>(r_d, aDO, aV_of(j));  // dP(j) = dO V^T
+      auto aK_of = [&](int j) { return smem_u32(smem + (2 + j % 3) * Cfg::kTileBytes); };
+      auto issue_s = [&](int j) {
+        if (!mbar_wait(&k_full[j % 3], static_cast<uint32_t>(j / 3) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
+        tc_fence_after();
+        bwd_mma_scores<D>(tmem + (j & 1) * 128, aQ, aK_of(j));  // S(j) = Q K^T
+        umma_commit(&s_ready[j & 1]);
+        return true;
+      };
+      auto issue_dp = [&](int j) {
+        if (!mbar_wait(&v_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
+        tc_fence_after();
+        bwd_mma_scores<D>(tmem + Cfg::kTmDp, aDO, smem_u32(smem + (5 + (j & 1)) * Cfg::kTileBytes));  // dP(j) = dO V^T
         umma_commit(&dp_ready);
+        umma_commit(&v_empty[j & 1]);
+        return true;
+      };
+      if (ok && n_j > 0) ok = issue_s(0) && issue_dp(0) && (n_j < 2 || issue_s(1));
+      for (int j = 0; ok && j < n_j; ++j) {
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(j) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
-        if (j + 1 < n_j) {
-          if (!mbar_wait(&full[(j + 1) & 1], static_cast<uint32_t>((j + 1) >> 1) & 1u, abort_p, kBwdWaitTimeoutNs))
-            break;
-          tc_fence_after();
-          bwd_mma_scores<D>(r_d, aQ, aK_of(j + 1));
-          umma_commit(&s_ready);
-        }
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aK_of(j), j > 0);  // dQ += dS K
-        umma_commit(&empty[j & 1]);
+        if (j + 1 < n_j && !issue_dp(j + 1)) break;
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmDq, tmem + (j & 1) * 128, 0, aK_of(j), j > 0);  // dQ += dS K
+        umma_commit(&k_empty[j % 3]);
+        if (j + 2 < n_j && !issue_s(j + 2)) break;
       }
       umma_commit(&acc_done);
     }
@@ -504,13 +528,16 @@ __global__ void __launch_bounds__(320, 1)
     const size_t r = (static_cast<size_t>(b) * p.Hq + h) * p.Tq + (q_ok ? q : 0);
     const float lse2 = q_ok ? p.lse[r] * kLog2e : INFINITY;  // rows past Tq: P = 0
     const float dl = q_ok ? p.delta[r] : 0.f;
+    const float2 c2 = make_float2(p.c, p.c), nl2 = make_float2(-lse2, -lse2), ndl2 = make_float2(-dl, -dl);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float c = p.c;
+    const uint32_t r_d = tmem + lane_off + Cfg::kTmDp;
     bool ok = true;
     for (int j = 0; j < n_j; ++j) {
-      const uint32_t r_s = tmem + lane_off + (j & 1) * 128, r_d = tmem + lane_off + ((j + 1) & 1) * 128;
+      const uint32_t r_s = tmem + lane_off + (j & 1) * 128;
+      // every key of the block is visible to every row of the query block: no mask
+      const bool full = (j + 1) * 128 <= p.Tk && (!p.causal || j * 128 + 127 <= i0);
       float pv[64];  // this thread's 64 probabilities, kept between the two phases
-      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(j) & 1u, abort_p,
+      if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
@@ -521,10 +548,17 @@ __global__ void __launch_bounds__(320, 1)
           uint32_t sr[32];
           tmem_ld32(r_s + k0, sr);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int key = j * 128 + k0 + k;
-            const bool vis = key < p.Tk && (!p.causal || key <= q);
-            pv[cc * 32 + k] = vis ? ex2_approx(__uint_as_float(sr[k]) * c - lse2) : 0.f;
+          for (int k = 0; k < 32; k += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nl2);
+            pv[cc * 32 + k] = ex2_approx(x.x);
+            pv[cc * 32 + k + 1] = ex2_approx(x.y);
+          }
+          if (!full) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int key = j * 128 + k0 + k;
+              if (!(key < p.Tk && (!p.causal || key <= q))) pv[cc * 32 + k] = 0.f;
+            }
           }
         }
       }
@@ -540,9 +574,11 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(r_d + k0, dr);
           uint32_t dd[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            dd[k] = pack_bf16x2(pv[cc * 32 + 2 * k] * (__uint_as_float(dr[2 * k]) - dl),
-                                pv[cc * 32 + 2 * k + 1] * (__uint_as_float(dr[2 * k + 1]) - dl));
+          for (int k = 0; k < 16; ++k) {
+            const float2 g = __fmul2_rn(make_float2(pv[cc * 32 + 2 * k], pv[cc * 32 + 2 * k + 1]),
+                                        __fadd2_rn(make_float2(__uint_as_float(dr[2 * k]), __uint_as_float(dr[2 * k + 1])), ndl2));
+            dd[k] = pack_bf16x2(g.x, g.y);
+          }
           tmem_st16(r_s + half * 64 + cc * 16, dd);
         }
         tmem_st_wait();
@@ -553,7 +589,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
     tc_fence_after();
-    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, p.scale, ok && n_j > 0, q_ok && (ok || n_j == 0),
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmDq, p.scale, ok && n_j > 0, q_ok && (ok || n_j == 0),
                      p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D, half);
     tc_fence_before();
   }
@@ -609,14 +645,14 @@ static cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, co
   *launched = 1;
   err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytesDq);
   if (err != cudaSuccess) return err;
   const dim3 g_kv((p.Tk + 127) / 128, p.B * p.Hkv);
   bwd_dkdv_kernel<D><<<g_kv, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   *launched = 2;
   const dim3 g_q((p.Tq + 127) / 128, p.B * p.Hq);
-  bwd_dq_kernel<D><<<g_q, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  bwd_dq_kernel<D><<<g_q, Cfg::kThreads, Cfg::kSmemBytesDq, stream>>>(mq, mk, mv, mdo, p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   *launched = 3;
   return cudaSuccess;
