@@ -421,86 +421,76 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads, 3)
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
-// One CTA per (sequence, query head): the weights 2^(m_s - M) of the non-empty splits
-// are computed once in shared memory, then every thread (one output element) sums its
-// column of partials in split order, so the result is deterministic for a given split count.
+// One CTA of D/64 warps per (sequence, query head); warp w owns output elements [64 w, 64 w + 64),
+// two per lane. The partials of up to 32 splits are loaded in one go, together with the sequence
+// length: a split past the length was never written and is dropped by predicate (its bytes are
+// inside the workspace, so reading them is harmless), which puts every load of a group in flight
+// before the first result is needed. The splits are merged in split order (lane t of the warp
+// owns split g0 + t's weight); with more than 32 splits each group of 32 is merged into a running
+// (M, l, o) by the same rescaling rule. The result is deterministic for a given split count.
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ o_part,
-                                                          const float* __restrict__ ml_part,
-                                                          const int* __restrict__ seqlens,
-                                                          __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                          int Hq, int S, int C, int Lcap) {
-  constexpr int kMaxSplitsInSmem = 1024;
-  __shared__ float w_s[kMaxSplitsInSmem];
-  __shared__ float red[D / 32];
-  __shared__ float Ms, Ls;
+__global__ void __launch_bounds__(D / 2) decode_combine_kernel(const float* __restrict__ o_part,
+                                                              const float* __restrict__ ml_part,
+                                                              const int* __restrict__ seqlens,
+                                                              __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                              int Hq, int S, int C, int Lcap) {
+  constexpr int kGroup = 32;
   // launched as a programmatic dependent of the split kernel: wait until that grid has
   // completed and its writes are visible (a no-op without such a dependency)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / Hq;
-  int L = seqlens[b];
-  L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
-  const int nsplit = min(S, (L + C - 1) / C);
-  const int e = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = warp * 64 + 2 * lane;
   const float* ml = ml_part + static_cast<size_t>(bh) * S * 2;
-  const float* op = o_part + static_cast<size_t>(bh) * S * D;
-  // M = max_s m_s (block reduction)
-  float mloc = -INFINITY;
-  for (int s = e; s < nsplit; s += D) mloc = fmaxf(mloc, ml[2 * s]);
+  const float* op = o_part + static_cast<size_t>(bh) * S * D + e0;
+  const int L_raw = seqlens[b];
+  float M = -INFINITY, lsum = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
+  for (int g0 = 0; g0 < S; g0 += kGroup) {
+    const int cnt = min(kGroup, S - g0);  // splits of this group inside the workspace
+    float2 mlv = make_float2(-INFINITY, 0.f);
+    if (lane < cnt) mlv = *reinterpret_cast<const float2*>(ml + 2 * (g0 + lane));
+    float2 v[kGroup];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xFFFFFFFFu, mloc, off));
-  if ((e & 31) == 0) red[e >> 5] = mloc;
-  __syncthreads();
-  if (e == 0) {
-    float M = -INFINITY;
-    for (int w = 0; w < D / 32; ++w) M = fmaxf(M, red[w]);
-    Ms = M;
+    for (int t = 0; t < kGroup; ++t)
+      v[t] = t < cnt ? *reinterpret_cast<const float2*>(op + static_cast<size_t>(g0 + t) * D) : make_float2(0.f, 0.f);
+    const int L = L_raw < 0 ? 0 : (L_raw > Lcap ? Lcap : L_raw);
+    const int nsplit = min(S, (L + C - 1) / C);
+    if (g0 >= nsplit) break;
+    const int valid = min(kGroup, nsplit - g0);  // splits of this group that were written
+    const bool mine = lane < valid;
+    float mg = mine ? mlv.x : -INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
+    const float M_new = fmaxf(M, mg);
+    if (M_new == -INFINITY) continue;  // nothing seen yet (every written split so far was empty)
+    const float w = mine ? ex2_approx(mlv.x - M_new) : 0.f;
+    float lp = w * (mine ? mlv.y : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(0xFFFFFFFFu, lp, off);
+    const float r = ex2_approx(M - M_new);  // 0 on the first group (M = -inf)
+    float2 a = make_float2(acc.x * r, acc.y * r);
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) {
+      const float wt = __shfl_sync(0xFFFFFFFFu, w, t);
+      if (t < valid) {
+        a.x = fmaf(wt, v[t].x, a.x);
+        a.y = fmaf(wt, v[t].y, a.y);
+      }
+    }
+    acc = a;
+    lsum = fmaf(lsum, r, lp);
+    M = M_new;
   }
-  __syncthreads();
-  const float M = Ms;
-  if (nsplit == 0 || M == -INFINITY) {
-    o[static_cast<size_t>(bh) * D + e] = __float2bfloat16_rn(0.f);
-    if (e == 0 && lse != nullptr) lse[bh] = -INFINITY;
+  __nv_bfloat16* orow = o + static_cast<size_t>(bh) * D + e0;
+  if (M == -INFINITY) {  // no key: O = 0, LSE = -inf
+    *reinterpret_cast<uint32_t*>(orow) = 0u;
+    if (threadIdx.x == 0 && lse != nullptr) lse[bh] = -INFINITY;
     return;
   }
-  const bool in_smem = nsplit <= kMaxSplitsInSmem;
-  // weights and the weighted sum of l: thread e takes splits e, e + D, ... (fixed order),
-  // then a fixed-shape block reduction, so the result does not depend on timing
-  float lpart = 0.f;
-  for (int s = e; s < nsplit; s += D) {
-    const float w = ex2_approx(ml[2 * s] - M);
-    if (in_smem) w_s[s] = w;
-    lpart = fmaf(w, ml[2 * s + 1], lpart);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xFFFFFFFFu, lpart, off);
-  __syncthreads();  // red[] reuse and w_s complete
-  if ((e & 31) == 0) red[e >> 5] = lpart;
-  __syncthreads();
-  if (e == 0) {
-    float lsum = 0.f;
-    for (int w = 0; w < D / 32; ++w) lsum += red[w];
-    Ls = lsum;
-  }
-  float acc = 0.f;
-  int s = 0;
-  if (in_smem) {
-    for (; s + 4 <= nsplit; s += 4) {  // fixed order, four independent loads in flight
-      const float a0 = op[static_cast<size_t>(s) * D + e], a1 = op[static_cast<size_t>(s + 1) * D + e];
-      const float a2 = op[static_cast<size_t>(s + 2) * D + e], a3 = op[static_cast<size_t>(s + 3) * D + e];
-      acc = fmaf(w_s[s], a0, acc);
-      acc = fmaf(w_s[s + 1], a1, acc);
-      acc = fmaf(w_s[s + 2], a2, acc);
-      acc = fmaf(w_s[s + 3], a3, acc);
-    }
-  }
-  for (; s < nsplit; ++s)
-    acc = fmaf(in_smem ? w_s[s] : ex2_approx(ml[2 * s] - M), op[static_cast<size_t>(s) * D + e], acc);
-  __syncthreads();
-  const float lsum = Ls;
-  o[static_cast<size_t>(bh) * D + e] = __float2bfloat16_rn(acc / lsum);
-  if (e == 0 && lse != nullptr) lse[bh] = (M + log2f(lsum)) * 0.69314718055994530942f;
+  *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc.x / lsum, acc.y / lsum);
+  if (threadIdx.x == 0 && lse != nullptr) lse[bh] = (M + log2f(lsum)) * 0.69314718055994530942f;
 }
 
 template <int D, int G, int EB>
@@ -560,7 +550,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const f
   // kernel orders its reads after the split kernel's writes.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(Hq));
-  cfg.blockDim = dim3(static_cast<unsigned>(d));
+  cfg.blockDim = dim3(static_cast<unsigned>(d / 2));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

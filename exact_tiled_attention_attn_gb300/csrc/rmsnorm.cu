@@ -116,6 +116,10 @@ template <int NSEG, int VPL, bool RES>
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const uint4* __restrict__ x, const uint4* __restrict__ res,
                                                            const uint4* __restrict__ w, uint4* __restrict__ y,
                                                            uint4* __restrict__ h, int T, int D, float eps) {
+  // launched with programmatic stream serialisation (see launch_shape): wait until the previous
+  // kernel on the stream has completed and its writes are visible, then let the next launch be set up
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int kRounds = NSEG == 8 ? 4 : 1;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -162,6 +166,10 @@ template <int NSEG, int VPL, bool RES>
 __global__ void __launch_bounds__(32 * kNormSplitWarps) rmsnorm_split_kernel(
     const uint4* __restrict__ x, const uint4* __restrict__ res, const uint4* __restrict__ w, uint4* __restrict__ y,
     uint4* __restrict__ h, int D, float eps) {
+  // launched with programmatic stream serialisation (see launch_shape): wait until the previous
+  // kernel on the stream has completed and its writes are visible, then let the next launch be set up
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float seg_sum[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row = blockIdx.x;
@@ -200,14 +208,29 @@ static cudaError_t launch_shape(const void* x, const void* r, const void* w, voi
   const uint4* wp = static_cast<const uint4*>(w);
   uint4* yp = static_cast<uint4*>(y);
   uint4* hp = static_cast<uint4*>(h);
+  // Programmatic stream serialisation: the grid's CTAs may be placed while the previous kernel on
+  // the stream drains (griddepcontrol.wait in the kernel orders every read after its completion),
+  // which hides most of the launch gap of this short, latency-bound kernel.
+  cudaLaunchConfig_t cfg = {};
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err;
   if (T <= kNormSplitMaxRows) {
-    rmsnorm_split_kernel<NSEG, VPL, RES><<<T, 32 * kNormSplitWarps, 0, s>>>(xp, rp, wp, yp, hp, D, eps);
+    cfg.gridDim = dim3(static_cast<unsigned>(T));
+    cfg.blockDim = dim3(32 * kNormSplitWarps);
+    err = cudaLaunchKernelEx(&cfg, rmsnorm_split_kernel<NSEG, VPL, RES>, xp, rp, wp, yp, hp, D, eps);
   } else {
     const int rows_per_block = 8;
-    rmsnorm_warp_kernel<NSEG, VPL, RES>
-        <<<(T + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, s>>>(xp, rp, wp, yp, hp, T, D, eps);
+    cfg.gridDim = dim3(static_cast<unsigned>((T + rows_per_block - 1) / rows_per_block));
+    cfg.blockDim = dim3(32 * rows_per_block);
+    err = cudaLaunchKernelEx(&cfg, rmsnorm_warp_kernel<NSEG, VPL, RES>, xp, rp, wp, yp, hp, T, D, eps);
   }
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 // VPL = vectors per virtual lane per segment, rounded up to a power of two.
