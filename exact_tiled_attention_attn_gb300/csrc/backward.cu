@@ -69,29 +69,37 @@ struct BwdParams {
   float scale;
 };
 
-// D[128 x 128] = A_tile . B_tile^T over K = D (both tiles 128 rows x D, K-major)
+// Shared-memory descriptors of a tile at byte offset `off` from the descriptor of tile 0: the start
+// address field holds address >> 4 in the low 14 bits, and no address here reaches 2^18, so adding
+// off >> 4 to the whole descriptor moves the start and nothing else. The issuing thread forms each
+// MMA's descriptors with one add instead of rebuilding them.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t desc0, uint32_t off_bytes) { return desc0 + (off_bytes >> 4); }
+
+// D[128 x 128] = A_tile . B_tile^T over K = D (both tiles 128 rows x D, K-major; a, b are their
+// descriptors with LBO 16, SBO 1024)
 template <int D>
-__device__ __forceinline__ void bwd_mma_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+__device__ __forceinline__ void bwd_mma_scores(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   using Cfg = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32;
-    umma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024), make_sdesc_sw128(b_smem + off, 16, 1024),
-            Cfg::kIdescS, kk > 0 ? 1u : 0u);
+    const uint32_t off16 = ((kk >> 2) * Cfg::kBoxBytes + (kk & 3) * 32) >> 4;
+    umma_ss(d_tmem, a_desc + off16, b_desc + off16, Cfg::kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
 // D[128 x D] (+)= A (TMEM, 128 rows x 128 bf16) . B (128 rows x D, MN-major), with A's bf16 pairs
 // in the layout the score region holds after the two compute phases: for each half h of the 128
 // columns, 32 columns at region + 64 h + a_off (a_off 0: P^T, 32: dS^T).
+// b_desc: the B tile's MN-major descriptor (LBO = one 64-column box, SBO 1024); each K step of 16
+// rows moves it by 2048 bytes.
 template <int D>
 __device__ __forceinline__ void bwd_mma_accumulate_split(uint32_t d_tmem, uint32_t region, uint32_t a_off,
-                                                         uint32_t b_smem, bool accumulate) {
+                                                         uint64_t b_desc, bool accumulate) {
   using Cfg = BwdCfg<D>;
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    umma_ts(d_tmem, region + (kk >> 2) * 64 + a_off + (kk & 3) * 8,
-            make_sdesc_sw128(b_smem + kk * 2048, Cfg::kBoxBytes, 1024), Cfg::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts(d_tmem, region + (kk >> 2) * 64 + a_off + (kk & 3) * 8, b_desc + kk * (2048 >> 4), Cfg::kIdescAcc,
+            (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Half `half` (columns [half*D/2, (half+1)*D/2)) of one row (this thread's TMEM lane) of a
@@ -247,9 +255,15 @@ __global__ void __launch_bounds__(320, 1)
       // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
       // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
       bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      auto aQ_of = [&](int it) { return smem_u32(smem + (2 + 2 * (it & 1)) * Cfg::kTileBytes); };
-      auto aDO_of = [&](int it) { return smem_u32(smem + (3 + 2 * (it & 1)) * Cfg::kTileBytes); };
+      const uint64_t aK = make_sdesc_sw128(smem_u32(sK), 16, 1024), aV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+      // descriptors of the stage tiles: Q(i) at tile 2 + 2 (i & 1), dO(i) at 3 + 2 (i & 1); K-major for the
+      // score GEMMs, MN-major (LBO one box) as the B operand of dV and dK
+      const uint64_t q_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
+      const uint64_t q_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
+      auto aQ_of = [&](int it) { return sdesc_at(q_k0, (2 * (it & 1)) * Cfg::kTileBytes); };
+      auto aDO_of = [&](int it) { return sdesc_at(q_k0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
+      auto bQ_of = [&](int it) { return sdesc_at(q_mn0, (2 * (it & 1)) * Cfg::kTileBytes); };
+      auto bDO_of = [&](int it) { return sdesc_at(q_mn0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
       if (ok && n_it > 0) {
         ok = mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
         if (ok) {
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(320, 1)
         // dV needs only P^T: it runs while phase 2 forms dS^T in the other columns of the region
         if (!mbar_wait(&p1_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, aDO_of(it), it > 0);   // dV += P^T dO
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, bDO_of(it), it > 0);   // dV += P^T dO
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
         if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(320, 1)
           bwd_mma_scores<D>(r_d, aK, aQ_of(it + 1));
           umma_commit(&s_ready);
         }
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, aQ_of(it), it > 0);   // dK += dS^T Q
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, bQ_of(it), it > 0);   // dK += dS^T Q
         umma_commit(&empty[it & 1]);
       }
       umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
@@ -490,8 +504,13 @@ __global__ void __launch_bounds__(320, 1)
       // tensor pipe runs one thread's MMAs in issue order). S(j + 1) was issued a block earlier, so
       // phase 1 of block j + 1 starts at once and the tensor pipe has work during phase 2.
       bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      auto aK_of = [&](int j) { return smem_u32(smem + (2 + j % 3) * Cfg::kTileBytes); };
+      const uint64_t aQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024), aDO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
+      // K(j): K-major for S, MN-major (LBO one box) as the B operand of dQ; V(j): K-major for dP
+      const uint64_t k_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
+      const uint64_t k_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
+      auto aK_of = [&](int j) { return sdesc_at(k_k0, (j % 3) * Cfg::kTileBytes); };
+      auto bK_of = [&](int j) { return sdesc_at(k_mn0, (j % 3) * Cfg::kTileBytes); };
+      auto aV_of = [&](int j) { return sdesc_at(k_k0, (3 + (j & 1)) * Cfg::kTileBytes); };
       auto issue_s = [&](int j) {
         if (!mbar_wait(&k_full[j % 3], static_cast<uint32_t>(j / 3) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
         tc_fence_after();
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(320, 1)
       auto issue_dp = [&](int j) {
         if (!mbar_wait(&v_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
         tc_fence_after();
-        bwd_mma_scores<D>(tmem + Cfg::kTmDp, aDO, smem_u32(smem + (5 + (j & 1)) * Cfg::kTileBytes));  // dP(j) = dO V^T
+        bwd_mma_scores<D>(tmem + Cfg::kTmDp, aDO, aV_of(j));  // dP(j) = dO V^T
         umma_commit(&dp_ready);
         umma_commit(&v_empty[j & 1]);
         return true;
@@ -512,7 +531,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(&p_ready, static_cast<uint32_t>(j) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
         tc_fence_after();
         if (j + 1 < n_j && !issue_dp(j + 1)) break;
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmDq, tmem + (j & 1) * 128, 0, aK_of(j), j > 0);  // dQ += dS K
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmDq, tmem + (j & 1) * 128, 0, bK_of(j), j > 0);  // dQ += dS K
         umma_commit(&k_empty[j % 3]);
         if (j + 2 < n_j && !issue_s(j + 2)) break;
       }
