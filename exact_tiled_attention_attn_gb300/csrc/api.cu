@@ -107,7 +107,13 @@ int attn_decode_default_splits(int B, int Hkv, int Lcap) {
   // splits for ~4 thread blocks per SM of a 152-SM part when the batch is small.
   int s = (Lcap + 1023) / 1024;
   const long long want = (4LL * 152 + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
-  if (s < want) s = static_cast<int>(want);
+  if (s < want) s = want > (1 << 20) ? (1 << 20) : static_cast<int>(want);
+  // Rounded down to a power of two: with a power-of-two cache length every chunk is then a whole
+  // number of the kernel's 64-row stages (measured, B16 Hkv8 d128: Lcap 2048, 4 splits 23.7 us per
+  // step vs 28.3 us with 5; Lcap 8192, 8 splits 75.3 vs 90.6 with 6; Lcap 32768, 32 splits best).
+  int p2 = 1;
+  while (p2 <= s / 2) p2 *= 2;
+  s = p2;
   const int smax = (Lcap + 15) / 16;
   if (s > smax) s = smax;
   return s < 1 ? 1 : s;
