@@ -46,8 +46,8 @@ WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 # ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md,
 # with the SHA-256 of the kernel source it was taken with: the figure is reported only while
 # that source is unchanged.
-PREFILL_TRAFFIC = {"bytes": 343813120 + 95751680,
-                   "prefill_cu_sha256": "907c8818e7eeb9d0e26d4b72f8a47f26b8368c3870cd687790a9915494fe4116"}
+PREFILL_TRAFFIC = {"bytes": 348698368 + 94247424,
+                   "prefill_cu_sha256": "ac5507e5c8398274bc66cf7a2f464edd09c3375f54872300994bf8ce3d427e21"}
 
 
 def prefill_traffic():

@@ -622,36 +622,6 @@ __global__ void __launch_bounds__(320, 1)
 // ------------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------------
-typedef CUresult (*PFN_encodeTiledBwd)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static PFN_encodeTiledBwd bwd_encode_fn() {
-  static PFN_encodeTiledBwd fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_encodeTiledBwd>(ptr);
-  }
-  return fn;
-}
-
-// [Z, rows, D] bf16, box 64 columns x 128 rows x 1, 128-byte swizzle, rows past the end read as zero
-static bool bwd_map_3d(CUtensorMap* map, const void* base, int D, int rows, int Z) {
-  PFN_encodeTiledBwd enc = bwd_encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(Z)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 static cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                                 const CUtensorMap& mdo, const __nv_bfloat16* o, const __nv_bfloat16* dout,
@@ -682,8 +652,8 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
                             int d, int causal, float scale, void* workspace, cudaStream_t stream, int* launched) {
   *launched = 0;
   CUtensorMap mq, mk, mv, mdo;
-  if (!bwd_map_3d(&mq, q, d, Tq, B * Hq) || !bwd_map_3d(&mk, k, d, Tk, B * Hkv) ||
-      !bwd_map_3d(&mv, v, d, Tk, B * Hkv) || !bwd_map_3d(&mdo, dout, d, Tq, B * Hq))
+  if (!encode_bf16_tile_map(&mq, q, d, Tq, B * Hq) || !encode_bf16_tile_map(&mk, k, d, Tk, B * Hkv) ||
+      !encode_bf16_tile_map(&mv, v, d, Tk, B * Hkv) || !encode_bf16_tile_map(&mdo, dout, d, Tq, B * Hq))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.lse = lse;

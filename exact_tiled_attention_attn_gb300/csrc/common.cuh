@@ -306,4 +306,8 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads)
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Host: a 3-D TMA map over a [Z, rows, D] bf16 tensor, box 64 columns x 128 rows x 1, 128-byte
+// swizzle, rows past the end read as zero (tmap.cu). False if the driver cannot encode it.
+bool encode_bf16_tile_map(CUtensorMap* map, const void* base, int D, int rows, int Z);
+
 }  // namespace gb300

@@ -535,38 +535,6 @@ __global__ void __launch_bounds__(352, 1)
 // --------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // --------------------------------------------------------------------------------------
-typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static PFN_encodeTiled get_encode_fn() {
-  static PFN_encodeTiled fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_encodeTiled>(ptr);
-  }
-  return fn;
-}
-
-// 3-D map over a [Z, rows, D] bf16 tensor, box = 64 columns x 128 rows x 1, 128-byte swizzle,
-// out-of-range rows read as zero.
-static bool make_map_3d(CUtensorMap* map, const void* base, int D, int rows, int Z) {
-  PFN_encodeTiled enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(Z)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Streaming multiprocessors of the current device (queried once per device).
 static int sm_count() {
   static int cached[64] = {0};
@@ -603,8 +571,8 @@ static cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, co
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                             int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
-  if (!make_map_3d(&mq, q, d, Tq, B * Hq) || !make_map_3d(&mk, k, d, Tk, B * Hkv) ||
-      !make_map_3d(&mv, v, d, Tk, B * Hkv))
+  if (!encode_bf16_tile_map(&mq, q, d, Tq, B * Hq) || !encode_bf16_tile_map(&mk, k, d, Tk, B * Hkv) ||
+      !encode_bf16_tile_map(&mv, v, d, Tk, B * Hkv))
     return cudaErrorInvalidValue;
   PrefillParams p;
   p.o = static_cast<__nv_bfloat16*>(o);
