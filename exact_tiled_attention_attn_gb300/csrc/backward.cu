@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
       const int h = kvh * p.g + it / n_i;
       const int i0 = (i_first + it % n_i) * 128;
       // every key of the block is visible to every query of the query block: no mask
-      const bool full = j0 + 128 <= p.Tk && (!p.causal || j0 + 127 <= i0);
+      const bool unmasked = j0 + 128 <= p.Tk && (!p.causal || j0 + 127 <= i0);
       named_bar_sync(1, 256);  // the previous block's readers of nl_s / ndl_s are done
       {
         const int q = i0 + row;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(320, 1)
             pv[cc * 32 + 4 * v4 + 2] = ex2_approx(x23.x);
             pv[cc * 32 + 4 * v4 + 3] = ex2_approx(x23.y);
           }
-          if (!full) {
+          if (!unmasked) {
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               if (!(key_ok && (!p.causal || key <= i0 + q0 + k))) pv[cc * 32 + k] = 0.f;
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int j = 0; j < n_j; ++j) {
       const uint32_t r_s = tmem + lane_off + (j & 1) * 128;
       // every key of the block is visible to every row of the query block: no mask
-      const bool full = (j + 1) * 128 <= p.Tk && (!p.causal || j * 128 + 127 <= i0);
+      const bool unmasked = (j + 1) * 128 <= p.Tk && (!p.causal || j * 128 + 127 <= i0);
       float pv[64];  // this thread's 64 probabilities, kept between the two phases
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(320, 1)
             pv[cc * 32 + k] = ex2_approx(x.x);
             pv[cc * 32 + k + 1] = ex2_approx(x.y);
           }
-          if (!full) {
+          if (!unmasked) {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int key = j * 128 + k0 + k;
