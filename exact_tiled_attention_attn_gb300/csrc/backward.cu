@@ -34,6 +34,20 @@
 namespace gb300 {
 
 constexpr uint64_t kBwdWaitTimeoutNs = 2000000000ull;  // 2 s per wait
+// Hardware named barriers (0 is __syncthreads; the dK/dV kernel's compute warps use 1 among
+// themselves). The MMA thread learns of every event it waits for through these, not through an
+// mbarrier wait of its own: under MMA load such a wait costs it a few hundred clocks even on a
+// phase that has already completed, and the tensor pipe idles meanwhile.
+//  * kBwdBarP1 / kBwdBarP: the 8 compute warps arrive once per block (P^T written; dS written),
+//    the MMA warp syncs (count 256 + 32). An arrival for block i + 1 needs a GEMM that is only
+//    issued after the sync for block i, so arrivals never run a generation ahead.
+//  * kBwdBarGo / kBwdBarAck: a helper warp waits on the mbarriers of the streamed tiles and hands
+//    each completion to the MMA warp (Go), which acknowledges it (Ack) before the helper looks at
+//    the next one, so the two warps stay in lockstep.
+// Every arrival and sync runs once per block on every path, also after an abort (a bar.sync
+// cannot time out): the counts on the two sides are equal by construction.
+constexpr uint32_t kBwdBarP1 = 2, kBwdBarP = 3, kBwdBarGo = 4, kBwdBarAck = 5;
+constexpr uint32_t kBwdComputeAndMma = 288, kBwdPair = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -41,7 +55,7 @@ struct BwdCfg {
   static constexpr int kBoxBytes = 128 * 128;            // 128 rows x 64 bf16 columns, 128-byte swizzle
   static constexpr int kNumBox = D / 64;
   static constexpr int kTileBytes = kNumBox * kBoxBytes;  // 128 rows x D
-  static constexpr int kThreads = 320;                    // warps 0-7 compute, 8 TMA, 9 MMA
+  static constexpr int kThreads = 352;                    // warps 0-7 compute, 8 TMA, 9 MMA, 10 wait helper
   // 2 resident tiles + 2 stages x 2 tiles; at least 116 KB so that one CTA runs per SM (each
   // allocates all 512 TMEM columns)
   static constexpr int kSmemBytes = (6 * kTileBytes + 1024) > 116 * 1024 ? (6 * kTileBytes + 1024) : 116 * 1024;
@@ -162,7 +176,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // dK, dV: one CTA per (key block, K/V head)
 // ------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams p) {
@@ -172,7 +186,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::kTileBytes;
   // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
-  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, p1_ready, p_ready, acc_done;
+  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, acc_done;
   __shared__ __align__(16) float nl_s[128];   // -L log2(e) per query row, read as float4
   __shared__ __align__(16) float ndl_s[128];  // -D per query row
   __shared__ uint32_t tmem_holder;
@@ -195,8 +209,6 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&s_ready, 1);
     mbar_init(&dp_ready, 1);
-    mbar_init(&p1_ready, 8);
-    mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -244,56 +256,76 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- wait helper: Q(i), dO(i) of blocks 1 .. n-1 landed -> MMA warp ----------------
+    for (int it = 1; it < n_it; ++it) {
+      if (lane == 0 && !*abort_p)
+        mbar_wait(&full[it & 1], static_cast<uint32_t>(it >> 1) & 1u, abort_p, kBwdWaitTimeoutNs);
+      __syncwarp();
+      named_bar_arrive(kBwdBarGo, kBwdPair);
+      named_bar_sync(kBwdBarAck, kBwdPair);
+    }
   } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      // The two 128-column score regions swap roles every block: S^T(i) goes to region i & 1 and
-      // dP^T(i) to the other one. The compute warps turn S^T(i) into P^T(i) (phase 1, needs only
-      // S^T) and then, with dP^T(i), into dS^T(i) (phase 2), both kept inside S^T(i)'s region, so
-      // dP^T(i)'s region is free once phase 2 is done: S^T(i + 1) goes there while dV(i), dK(i)
-      // read P^T(i), dS^T(i), and dP^T(i + 1) follows into S^T(i)'s region (the tensor pipe runs
-      // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
-      // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
-      bool ok = n_it == 0 || mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs);
-      const uint64_t aK = make_sdesc_sw128(smem_u32(sK), 16, 1024), aV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
-      // descriptors of the stage tiles: Q(i) at tile 2 + 2 (i & 1), dO(i) at 3 + 2 (i & 1); K-major for the
-      // score GEMMs, MN-major (LBO one box) as the B operand of dV and dK
-      const uint64_t q_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
-      const uint64_t q_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
-      auto aQ_of = [&](int it) { return sdesc_at(q_k0, (2 * (it & 1)) * Cfg::kTileBytes); };
-      auto aDO_of = [&](int it) { return sdesc_at(q_k0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
-      auto bQ_of = [&](int it) { return sdesc_at(q_mn0, (2 * (it & 1)) * Cfg::kTileBytes); };
-      auto bDO_of = [&](int it) { return sdesc_at(q_mn0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
-      if (ok && n_it > 0) {
-        ok = mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
-        if (ok) {
-          tc_fence_after();
-          bwd_mma_scores<D>(tmem, aK, aQ_of(0));  // S^T(0) = K Q^T into region 0
-          umma_commit(&s_ready);
-        }
+    // ---------------- MMA issuer (the whole warp runs the loop for the named barriers; lane 0 issues) ----------------
+    // The two 128-column score regions swap roles every block: S^T(i) goes to region i & 1 and
+    // dP^T(i) to the other one. The compute warps turn S^T(i) into P^T(i) (phase 1, needs only
+    // S^T) and then, with dP^T(i), into dS^T(i) (phase 2), both kept inside S^T(i)'s region, so
+    // dP^T(i)'s region is free once phase 2 is done: S^T(i + 1) goes there while dV(i), dK(i)
+    // read P^T(i), dS^T(i), and dP^T(i + 1) follows into S^T(i)'s region (the tensor pipe runs
+    // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
+    // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
+    const uint64_t aK = make_sdesc_sw128(smem_u32(sK), 16, 1024), aV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+    // descriptors of the stage tiles: Q(i) at tile 2 + 2 (i & 1), dO(i) at 3 + 2 (i & 1); K-major for the
+    // score GEMMs, MN-major (LBO one box) as the B operand of dV and dK
+    const uint64_t q_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
+    const uint64_t q_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
+    auto aQ_of = [&](int it) { return sdesc_at(q_k0, (2 * (it & 1)) * Cfg::kTileBytes); };
+    auto aDO_of = [&](int it) { return sdesc_at(q_k0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
+    auto bQ_of = [&](int it) { return sdesc_at(q_mn0, (2 * (it & 1)) * Cfg::kTileBytes); };
+    auto bDO_of = [&](int it) { return sdesc_at(q_mn0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
+    // K, V and the first Q, dO tiles: the issuing thread's own waits, once per CTA. After a failed
+    // wait (or an abort) the handoffs below still run to the end; only the MMAs are skipped.
+    bool ok = true;
+    if (lane == 0 && n_it > 0) {
+      ok = mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs) && mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
+      if (ok) {
+        tc_fence_after();
+        bwd_mma_scores<D>(tmem, aK, aQ_of(0));  // S^T(0) = K Q^T into region 0
+        umma_commit(&s_ready);
       }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const uint32_t r_s = tmem + (it & 1) * 128, r_d = tmem + ((it + 1) & 1) * 128;
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+    for (int it = 0; it < n_it; ++it) {
+      const uint32_t r_s = tmem + (it & 1) * 128, r_d = tmem + ((it + 1) & 1) * 128;
+      if (lane == 0 && ok) {
         bwd_mma_scores<D>(r_d, aV, aDO_of(it));  // dP^T(i) = V dO^T
         umma_commit(&dp_ready);
-        // dV needs only P^T: it runs while phase 2 forms dS^T in the other columns of the region
-        if (!mbar_wait(&p1_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
+      }
+      // dV needs only P^T: it runs while phase 2 forms dS^T in the other columns of the region
+      __syncwarp();
+      named_bar_sync(kBwdBarP1, kBwdComputeAndMma);
+      if (lane == 0 && ok) {
         tc_fence_after();
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, bDO_of(it), it > 0);   // dV += P^T dO
-        if (!mbar_wait(&p_ready, static_cast<uint32_t>(it) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
-        tc_fence_after();
-        if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
-          if (!mbar_wait(&full[(it + 1) & 1], static_cast<uint32_t>((it + 1) >> 1) & 1u, abort_p, kBwdWaitTimeoutNs))
-            break;
+      }
+      __syncwarp();
+      named_bar_sync(kBwdBarP, kBwdComputeAndMma);
+      if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
+        named_bar_sync(kBwdBarGo, kBwdPair);     // Q(i + 1), dO(i + 1) are in shared memory
+        named_bar_arrive(kBwdBarAck, kBwdPair);
+        if (lane == 0 && ok) {
           tc_fence_after();
           bwd_mma_scores<D>(r_d, aK, aQ_of(it + 1));
           umma_commit(&s_ready);
         }
+      }
+      if (lane == 0 && ok) {
+        tc_fence_after();
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, bQ_of(it), it > 0);   // dK += dS^T Q
         umma_commit(&empty[it & 1]);
       }
-      umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
     }
+    if (lane == 0) umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
     __syncwarp();
   } else {
     // ---------------- compute warps: key row j0 + (t & 127) (TMEM lane), query half t >> 7 ----------------
@@ -357,7 +389,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p1_ready);  // P^T(i) is in TMEM (every block, also after a failed wait)
+      named_bar_arrive(kBwdBarP1, kBwdComputeAndMma);  // P^T(i) is in TMEM (every block, also after a failed wait)
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&dp_ready, static_cast<uint32_t>(it) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
       if (ok) {
@@ -388,7 +420,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready);  // every block, also after a failed wait
+      named_bar_arrive(kBwdBarP, kBwdComputeAndMma);  // dS^T(i) is in TMEM (every block, also after a failed wait)
     }
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
     tc_fence_after();
@@ -410,7 +442,7 @@ __global__ void __launch_bounds__(320, 1)
 // dQ: one CTA per (query block, query head)
 // ------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                   const BwdParams p) {
@@ -421,8 +453,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sDO = smem + Cfg::kTileBytes;
   // K(j) in tile 2 + j mod 3, V(j) in tile 5 + j mod 2. K is read by S(j) and, one block later, by
   // dQ(j), while S(j + 2) is already wanted: three K tiles are live at once.
-  __shared__ uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_ready[2], dp_ready, p_ready,
-      acc_done;
+  __shared__ uint64_t qd_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_ready[2], dp_ready, acc_done;
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
 
@@ -446,7 +477,6 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_ready[s], 1);
     }
     mbar_init(&dp_ready, 1);
-    mbar_init(&p_ready, 8);
     mbar_init(&acc_done, 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -495,48 +525,84 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ---------------- wait helper: V(j + 1), then K(j + 2), landed -> MMA warp, once per block j ----------------
+    for (int j = 0; j < n_j; ++j) {
+      if (j + 1 < n_j) {
+        if (lane == 0 && !*abort_p)
+          mbar_wait(&v_full[(j + 1) & 1], static_cast<uint32_t>((j + 1) >> 1) & 1u, abort_p, kBwdWaitTimeoutNs);
+        __syncwarp();
+        named_bar_arrive(kBwdBarGo, kBwdPair);
+        named_bar_sync(kBwdBarAck, kBwdPair);
+      }
+      if (j + 2 < n_j) {
+        if (lane == 0 && !*abort_p)
+          mbar_wait(&k_full[(j + 2) % 3], static_cast<uint32_t>((j + 2) / 3) & 1u, abort_p, kBwdWaitTimeoutNs);
+        __syncwarp();
+        named_bar_arrive(kBwdBarGo, kBwdPair);
+        named_bar_sync(kBwdBarAck, kBwdPair);
+      }
+    }
   } else if (warp == 9) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      // S(j) goes to region j & 1 and dP(j) always to [256, 384); phase 2 writes dS(j) inside S(j)'s
-      // region. Once phase 2 of block j is done: dP(j + 1) (phase 2 of block j + 1 waits for it
-      // first), dQ(j) += dS(j) K(j), and S(j + 2) into S(j)'s region after dQ(j) has read it (the
-      // tensor pipe runs one thread's MMAs in issue order). S(j + 1) was issued a block earlier, so
-      // phase 1 of block j + 1 starts at once and the tensor pipe has work during phase 2.
-      bool ok = n_j == 0 || mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs);
-      const uint64_t aQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024), aDO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
-      // K(j): K-major for S, MN-major (LBO one box) as the B operand of dQ; V(j): K-major for dP
-      const uint64_t k_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
-      const uint64_t k_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
-      auto aK_of = [&](int j) { return sdesc_at(k_k0, (j % 3) * Cfg::kTileBytes); };
-      auto bK_of = [&](int j) { return sdesc_at(k_mn0, (j % 3) * Cfg::kTileBytes); };
-      auto aV_of = [&](int j) { return sdesc_at(k_k0, (3 + (j & 1)) * Cfg::kTileBytes); };
-      auto issue_s = [&](int j) {
-        if (!mbar_wait(&k_full[j % 3], static_cast<uint32_t>(j / 3) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
+    // ---------------- MMA issuer (the whole warp runs the loop for the named barriers; lane 0 issues) ----------------
+    // S(j) goes to region j & 1 and dP(j) always to [256, 384); phase 2 writes dS(j) inside S(j)'s
+    // region. Once phase 2 of block j is done: dP(j + 1) (phase 2 of block j + 1 waits for it
+    // first), dQ(j) += dS(j) K(j), and S(j + 2) into S(j)'s region after dQ(j) has read it (the
+    // tensor pipe runs one thread's MMAs in issue order). S(j + 1) was issued a block earlier, so
+    // phase 1 of block j + 1 starts at once and the tensor pipe has work during phase 2.
+    const uint64_t aQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024), aDO = make_sdesc_sw128(smem_u32(sDO), 16, 1024);
+    // K(j): K-major for S, MN-major (LBO one box) as the B operand of dQ; V(j): K-major for dP
+    const uint64_t k_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
+    const uint64_t k_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
+    auto aK_of = [&](int j) { return sdesc_at(k_k0, (j % 3) * Cfg::kTileBytes); };
+    auto bK_of = [&](int j) { return sdesc_at(k_mn0, (j % 3) * Cfg::kTileBytes); };
+    auto aV_of = [&](int j) { return sdesc_at(k_k0, (3 + (j & 1)) * Cfg::kTileBytes); };
+    auto issue_s = [&](int j) {
+      tc_fence_after();
+      bwd_mma_scores<D>(tmem + (j & 1) * 128, aQ, aK_of(j));  // S(j) = Q K^T
+      umma_commit(&s_ready[j & 1]);
+    };
+    auto issue_dp = [&](int j) {
+      tc_fence_after();
+      bwd_mma_scores<D>(tmem + Cfg::kTmDp, aDO, aV_of(j));  // dP(j) = dO V^T
+      umma_commit(&dp_ready);
+      umma_commit(&v_empty[j & 1]);
+    };
+    // Q, dO, K(0), V(0), K(1): the issuing thread's own waits, once per CTA. After a failed wait (or an
+    // abort) the handoffs below still run to the end; only the MMAs are skipped.
+    bool ok = true;
+    if (lane == 0 && n_j > 0) {
+      ok = mbar_wait(&qd_full, 0, abort_p, kBwdWaitTimeoutNs) && mbar_wait(&k_full[0], 0, abort_p, kBwdWaitTimeoutNs);
+      if (ok) issue_s(0);
+      ok = ok && mbar_wait(&v_full[0], 0, abort_p, kBwdWaitTimeoutNs);
+      if (ok) issue_dp(0);
+      if (ok && n_j > 1) {
+        ok = mbar_wait(&k_full[1], 0, abort_p, kBwdWaitTimeoutNs);
+        if (ok) issue_s(1);
+      }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+    for (int j = 0; j < n_j; ++j) {
+      __syncwarp();
+      named_bar_sync(kBwdBarP, kBwdComputeAndMma);  // dS(j) is in TMEM, dP(j) consumed
+      if (j + 1 < n_j) {
+        named_bar_sync(kBwdBarGo, kBwdPair);  // V(j + 1) is in shared memory
+        named_bar_arrive(kBwdBarAck, kBwdPair);
+        if (lane == 0 && ok) issue_dp(j + 1);
+      }
+      if (lane == 0 && ok) {
         tc_fence_after();
-        bwd_mma_scores<D>(tmem + (j & 1) * 128, aQ, aK_of(j));  // S(j) = Q K^T
-        umma_commit(&s_ready[j & 1]);
-        return true;
-      };
-      auto issue_dp = [&](int j) {
-        if (!mbar_wait(&v_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_p, kBwdWaitTimeoutNs)) return false;
-        tc_fence_after();
-        bwd_mma_scores<D>(tmem + Cfg::kTmDp, aDO, aV_of(j));  // dP(j) = dO V^T
-        umma_commit(&dp_ready);
-        umma_commit(&v_empty[j & 1]);
-        return true;
-      };
-      if (ok && n_j > 0) ok = issue_s(0) && issue_dp(0) && (n_j < 2 || issue_s(1));
-      for (int j = 0; ok && j < n_j; ++j) {
-        if (!mbar_wait(&p_ready, static_cast<uint32_t>(j) & 1u, abort_p, kBwdWaitTimeoutNs)) break;
-        tc_fence_after();
-        if (j + 1 < n_j && !issue_dp(j + 1)) break;
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmDq, tmem + (j & 1) * 128, 0, bK_of(j), j > 0);  // dQ += dS K
         umma_commit(&k_empty[j % 3]);
-        if (j + 2 < n_j && !issue_s(j + 2)) break;
       }
-      umma_commit(&acc_done);
+      if (j + 2 < n_j) {
+        __syncwarp();
+        named_bar_sync(kBwdBarGo, kBwdPair);  // K(j + 2) is in shared memory
+        named_bar_arrive(kBwdBarAck, kBwdPair);
+        if (lane == 0 && ok) issue_s(j + 2);
+      }
     }
+    if (lane == 0) umma_commit(&acc_done);
     __syncwarp();
   } else {
     // ---------------- compute warps: query row i0 + (t & 127) (TMEM lane), key half t >> 7 ----------------
@@ -604,7 +670,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready);
+      named_bar_arrive(kBwdBarP, kBwdComputeAndMma);  // dS(j) is in TMEM (every block, also after a failed wait)
     }
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
     tc_fence_after();
