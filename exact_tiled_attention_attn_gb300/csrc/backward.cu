@@ -56,9 +56,9 @@ struct BwdCfg {
   static constexpr int kNumBox = D / 64;
   static constexpr int kTileBytes = kNumBox * kBoxBytes;  // 128 rows x D
   static constexpr int kThreads = 352;                    // warps 0-7 compute, 8 TMA, 9 MMA, 10 wait helper
-  // 2 resident tiles + 2 stages x 2 tiles; at least 116 KB so that one CTA runs per SM (each
-  // allocates all 512 TMEM columns)
-  static constexpr int kSmemBytes = (6 * kTileBytes + 1024) > 116 * 1024 ? (6 * kTileBytes + 1024) : 116 * 1024;
+  // 7 tiles in both kernels (2 resident, 3 + 2 streamed; see each kernel); at least 116 KB so that
+  // one CTA runs per SM (each allocates all 512 TMEM columns)
+  static constexpr int kSmemBytes = (7 * kTileBytes + 1024) > 116 * 1024 ? (7 * kTileBytes + 1024) : 116 * 1024;
   // [128 x 128] = A (128 x D, K-major) . B^T (B 128 x D, K-major)
   static constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false);
   // [128 x D] += A (TMEM, 128 x 128 bf16) . B (128 x D, MN-major)
@@ -66,9 +66,8 @@ struct BwdCfg {
   // dK/dV kernel TMEM columns: two 128-column score regions [0, 128) and [128, 256) that swap roles
   // every block, then the fp32 accumulators dV and dK
   static constexpr uint32_t kTmAcc0 = 256, kTmAcc1 = 256 + D;
-  // dQ kernel: Q and dO resident, three K stages and two V stages (7 tiles); TMEM: S in [0, 128) and
-  // [128, 256) by turns, dP in [256, 384), the fp32 dQ accumulator from 384
-  static constexpr int kSmemBytesDq = (7 * kTileBytes + 1024) > 116 * 1024 ? (7 * kTileBytes + 1024) : 116 * 1024;
+  // dQ kernel TMEM: S in [0, 128) and [128, 256) by turns, dP in [256, 384), the fp32 dQ
+  // accumulator from 384
   static constexpr uint32_t kTmDp = 256, kTmDq = 384;
 };
 
@@ -185,8 +184,10 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + Cfg::kTileBytes;
-  // stage s: Q at 2 + 2s, dO at 3 + 2s (in tiles)
-  __shared__ uint64_t kv_full, full[2], empty[2], s_ready, dp_ready, acc_done;
+  // Q(i) in tile 2 + i mod 3, dO(i) in tile 5 + i mod 2. Q(i) is read by S^T(i), issued a block
+  // early, and last by dK(i) at the end of block i; a third Q tile lets the copy of Q(i + 1) start a
+  // block before S^T(i + 1) needs it. dO(i) is last read by dV(i), in the middle of block i.
+  __shared__ uint64_t kv_full, q_full[3], q_empty[3], do_full[2], do_empty[2], s_ready, dp_ready, acc_done;
   __shared__ __align__(16) float nl_s[128];   // -L log2(e) per query row, read as float4
   __shared__ __align__(16) float ndl_s[128];  // -D per query row
   __shared__ uint32_t tmem_holder;
@@ -203,9 +204,13 @@ __global__ void __launch_bounds__(352, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&kv_full, 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
     }
     mbar_init(&s_ready, 1);
     mbar_init(&dp_ready, 1);
@@ -236,18 +241,21 @@ __global__ void __launch_bounds__(352, 1)
         tma_load_3d(sV + kb * Cfg::kBoxBytes, &tmV, &kv_full, kb * 64, j0, b * p.Hkv + kvh);
       }
       for (int it = 0; it < n_it; ++it) {
-        const int s = it & 1;
-        if (it >= 2 && !mbar_wait(&empty[s], static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
-          break;
+        const int sq = it % 3, sd = it & 1;
         const int h = kvh * p.g + it / n_i;
         const int i0 = (i_first + it % n_i) * 128;
-        uint8_t* sQ = smem + (2 + 2 * s) * Cfg::kTileBytes;
-        uint8_t* sDO = smem + (3 + 2 * s) * Cfg::kTileBytes;
-        mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
-        for (int kb = 0; kb < Cfg::kNumBox; ++kb) {
-          tma_load_3d(sQ + kb * Cfg::kBoxBytes, &tmQ, &full[s], kb * 64, i0, b * p.Hq + h);
-          tma_load_3d(sDO + kb * Cfg::kBoxBytes, &tmDO, &full[s], kb * 64, i0, b * p.Hq + h);
-        }
+        if (it >= 3 && !mbar_wait(&q_empty[sq], static_cast<uint32_t>(it / 3 - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+          break;
+        uint8_t* sQ = smem + (2 + sq) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&q_full[sq], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sQ + kb * Cfg::kBoxBytes, &tmQ, &q_full[sq], kb * 64, i0, b * p.Hq + h);
+        if (it >= 2 && !mbar_wait(&do_empty[sd], static_cast<uint32_t>((it >> 1) - 1) & 1u, abort_p, kBwdWaitTimeoutNs))
+          break;
+        uint8_t* sDO = smem + (5 + sd) * Cfg::kTileBytes;
+        mbar_arrive_expect_tx(&do_full[sd], Cfg::kTileBytes);
+        for (int kb = 0; kb < Cfg::kNumBox; ++kb)
+          tma_load_3d(sDO + kb * Cfg::kBoxBytes, &tmDO, &do_full[sd], kb * 64, i0, b * p.Hq + h);
       }
       if (*abort_p) {  // let copies still in flight land before the CTA exits
         const uint64_t t0 = global_timer_ns();
@@ -259,8 +267,9 @@ __global__ void __launch_bounds__(352, 1)
   } else if (warp == 10) {
     // ---------------- wait helper: Q(i), dO(i) of blocks 1 .. n-1 landed -> MMA warp ----------------
     for (int it = 1; it < n_it; ++it) {
-      if (lane == 0 && !*abort_p)
-        mbar_wait(&full[it & 1], static_cast<uint32_t>(it >> 1) & 1u, abort_p, kBwdWaitTimeoutNs);
+      if (lane == 0 && !*abort_p &&
+          mbar_wait(&q_full[it % 3], static_cast<uint32_t>(it / 3) & 1u, abort_p, kBwdWaitTimeoutNs))
+        mbar_wait(&do_full[it & 1], static_cast<uint32_t>(it >> 1) & 1u, abort_p, kBwdWaitTimeoutNs);
       __syncwarp();
       named_bar_arrive(kBwdBarGo, kBwdPair);
       named_bar_sync(kBwdBarAck, kBwdPair);
@@ -275,19 +284,20 @@ __global__ void __launch_bounds__(352, 1)
     // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
     // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
     const uint64_t aK = make_sdesc_sw128(smem_u32(sK), 16, 1024), aV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
-    // descriptors of the stage tiles: Q(i) at tile 2 + 2 (i & 1), dO(i) at 3 + 2 (i & 1); K-major for the
+    // descriptors of the streamed tiles: Q(i) at tile 2 + i mod 3, dO(i) at 5 + i mod 2; K-major for the
     // score GEMMs, MN-major (LBO one box) as the B operand of dV and dK
     const uint64_t q_k0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), 16, 1024);
     const uint64_t q_mn0 = make_sdesc_sw128(smem_u32(smem + 2 * Cfg::kTileBytes), Cfg::kBoxBytes, 1024);
-    auto aQ_of = [&](int it) { return sdesc_at(q_k0, (2 * (it & 1)) * Cfg::kTileBytes); };
-    auto aDO_of = [&](int it) { return sdesc_at(q_k0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
-    auto bQ_of = [&](int it) { return sdesc_at(q_mn0, (2 * (it & 1)) * Cfg::kTileBytes); };
-    auto bDO_of = [&](int it) { return sdesc_at(q_mn0, (1 + 2 * (it & 1)) * Cfg::kTileBytes); };
+    auto aQ_of = [&](int it) { return sdesc_at(q_k0, (it % 3) * Cfg::kTileBytes); };
+    auto aDO_of = [&](int it) { return sdesc_at(q_k0, (3 + (it & 1)) * Cfg::kTileBytes); };
+    auto bQ_of = [&](int it) { return sdesc_at(q_mn0, (it % 3) * Cfg::kTileBytes); };
+    auto bDO_of = [&](int it) { return sdesc_at(q_mn0, (3 + (it & 1)) * Cfg::kTileBytes); };
     // K, V and the first Q, dO tiles: the issuing thread's own waits, once per CTA. After a failed
     // wait (or an abort) the handoffs below still run to the end; only the MMAs are skipped.
     bool ok = true;
     if (lane == 0 && n_it > 0) {
-      ok = mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs) && mbar_wait(&full[0], 0, abort_p, kBwdWaitTimeoutNs);
+      ok = mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs) && mbar_wait(&q_full[0], 0, abort_p, kBwdWaitTimeoutNs) &&
+           mbar_wait(&do_full[0], 0, abort_p, kBwdWaitTimeoutNs);
       if (ok) {
         tc_fence_after();
         bwd_mma_scores<D>(tmem, aK, aQ_of(0));  // S^T(0) = K Q^T into region 0
@@ -307,11 +317,12 @@ __global__ void __launch_bounds__(352, 1)
       if (lane == 0 && ok) {
         tc_fence_after();
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, bDO_of(it), it > 0);   // dV += P^T dO
+        umma_commit(&do_empty[it & 1]);  // dO(i) read for the last time
       }
       __syncwarp();
       named_bar_sync(kBwdBarP, kBwdComputeAndMma);
       if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
-        named_bar_sync(kBwdBarGo, kBwdPair);     // Q(i + 1), dO(i + 1) are in shared memory
+        named_bar_sync(kBwdBarGo, kBwdPair);     // Q(i + 1) and dO(i + 1) are in shared memory
         named_bar_arrive(kBwdBarAck, kBwdPair);
         if (lane == 0 && ok) {
           tc_fence_after();
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(352, 1)
       if (lane == 0 && ok) {
         tc_fence_after();
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, bQ_of(it), it > 0);   // dK += dS^T Q
-        umma_commit(&empty[it & 1]);
+        umma_commit(&q_empty[it % 3]);  // Q(i) read for the last time
       }
     }
     if (lane == 0) umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
@@ -700,14 +711,14 @@ static cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, co
   *launched = 1;
   err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytesDq);
+  err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   const dim3 g_kv((p.Tk + 127) / 128, p.B * p.Hkv);
   bwd_dkdv_kernel<D><<<g_kv, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   *launched = 2;
   const dim3 g_q((p.Tq + 127) / 128, p.B * p.Hq);
-  bwd_dq_kernel<D><<<g_q, Cfg::kThreads, Cfg::kSmemBytesDq, stream>>>(mq, mk, mv, mdo, p);
+  bwd_dq_kernel<D><<<g_q, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   *launched = 3;
   return cudaSuccess;

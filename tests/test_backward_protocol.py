@@ -131,37 +131,47 @@ def _run(agents, copies, mma_queue, on_mma, rnd, max_steps):
 
 def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_steps=400000):
     rnd = random.Random(seed)
-    kv_full, full = _MBar("kv_full"), [_MBar("full[0]"), _MBar("full[1]")]
-    empty = [_MBar("empty[0]"), _MBar("empty[1]")]
+    kv_full = _MBar("kv_full")
+    q_full, q_empty = [_MBar(f"q_full[{i}]") for i in range(3)], [_MBar(f"q_empty[{i}]") for i in range(3)]
+    do_full, do_empty = [_MBar(f"do_full[{i}]") for i in range(2)], [_MBar(f"do_empty[{i}]") for i in range(2)]
     s_ready, dp_ready, acc_done = _MBar("s_ready"), _MBar("dp_ready"), _MBar("acc_done")
     p1, pb = _NamedBar("P1", 288), _NamedBar("P", 288)
     go, ackb = _NamedBar("Go", 64), _NamedBar("Ack", 64)
     cbar = _NamedBar("compute", 256)
     copies, mma = [], []
-    reads = {}                      # stage load index -> MMAs still to read it
-    stage_load = [None, None]
+    reads = {}                      # (tile kind, block) -> MMAs still to read it
+    q_stage, do_stage = [None] * 3, [None] * 2
 
     def producer():
         kv_full.arrive(tx=1)
         copies.append((kv_full, 1))
         for it in range(n_it):
-            s = it & 1
+            sq, sd = it % 3, it & 1
+            if it >= 3:
+                yield ("m", q_empty[sq], it // 3 - 1)
+                if reads.get(("q", q_stage[sq]), 0):
+                    raise AssertionError("Q stage overwritten while still to be read")
+            q_stage[sq] = it
+            reads[("q", it)] = 2            # S^T(i), dK(i)
+            q_full[sq].arrive(tx=1)
+            copies.append((q_full[sq], 1))
+            yield None
             if it >= 2:
-                yield ("m", empty[s], (it >> 1) - 1)
-                prev = stage_load[s]
-                if reads.get(prev, 0):
-                    raise AssertionError(f"stage {s} overwritten while load {prev} is still to be read")
-            stage_load[s] = it
-            reads[it] = 4 if it + 0 < n_it else 0   # S^T(i), dP^T(i), dV(i), dK(i) read Q(i)/dO(i)
-            full[s].arrive(tx=1)
-            copies.append((full[s], 1))
+                yield ("m", do_empty[sd], (it >> 1) - 1)
+                if reads.get(("do", do_stage[sd]), 0):
+                    raise AssertionError("dO stage overwritten while still to be read")
+            do_stage[sd] = it
+            reads[("do", it)] = 2           # dP^T(i), dV(i)
+            do_full[sd].arrive(tx=1)
+            copies.append((do_full[sd], 1))
             yield None
 
     def helper():
         for it in range(1 + helper_skew, n_it + helper_skew):
             k = min(it, n_it - 1)
             if helper_wait:
-                yield ("m", full[k & 1], k >> 1)
+                yield ("m", q_full[k % 3], k // 3)
+                yield ("m", do_full[k & 1], k >> 1)
             go.arrive(10)
             if ack:
                 yield ("n", ackb, ackb.sync(10))
@@ -172,23 +182,25 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
             mma.append(("commit", acc_done))
             return
         yield ("m", kv_full, 0)
-        yield ("m", full[0], 0)
-        mma.append(("read", 0))
+        yield ("m", q_full[0], 0)
+        yield ("m", do_full[0], 0)
+        mma.append(("read", ("q", 0)))
         mma.append(("commit", s_ready))
         for it in range(n_it):
-            mma.append(("read", it))
+            mma.append(("read", ("do", it)))            # dP^T(i)
             mma.append(("commit", dp_ready))
             yield ("n", p1, p1.sync(9))
-            mma.append(("read", it))
+            mma.append(("read", ("do", it)))            # dV(i)
+            mma.append(("commit", do_empty[it & 1]))
             yield ("n", pb, pb.sync(9))
             if it + 1 < n_it:
                 yield ("n", go, go.sync(9))
                 if ack:
                     ackb.arrive(9)
-                mma.append(("read", it + 1))
+                mma.append(("read", ("q", it + 1)))     # S^T(i + 1)
                 mma.append(("commit", s_ready))
-            mma.append(("read", it))
-            mma.append(("commit", empty[it & 1]))
+            mma.append(("read", ("q", it)))             # dK(i)
+            mma.append(("commit", q_empty[it % 3]))
         mma.append(("commit", acc_done))
 
     def compute(w):
@@ -208,8 +220,10 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
         if kind == "commit":
             arg.arrive()
         else:
-            if (arg >> 1) not in full[arg & 1].done:
-                raise AssertionError(f"an MMA read Q/dO of block {arg} before its copy landed")
+            which, j = arg
+            landed = (j // 3) in q_full[j % 3].done if which == "q" else (j >> 1) in do_full[j & 1].done
+            if not landed:
+                raise AssertionError(f"an MMA read {which}({j}) before its copy landed")
             reads[arg] -= 1
 
     agents = [producer(), helper(), issuer()] + [compute(w) for w in range(8)]
