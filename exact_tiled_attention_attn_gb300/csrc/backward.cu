@@ -20,12 +20,14 @@
 //   bwd_dq_kernel      one CTA per (block of 128 queries, query head): walks the visible key
 //                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into S's columns, dQ += dS K.
 // Each kernel: warps 0-7 compute (warps w and w + 4 share TMEM lanes 32(w mod 4) .. + 31 and
-// take one half of the row's 128 columns each), warp 8 issues the TMA copies (two stages of the
-// walked operand pair), warp 9 issues the MMAs from one thread. Every handoff is an mbarrier
-// with a bounded wait. The two 128-column score regions swap roles every block, so the next
-// block's scores go into the region phase 2 has just consumed while this block's gradient
-// GEMMs run, and phase 1 of the next block overlaps them (recomputing S and dP in the dQ
-// kernel costs 2 of its 3 GEMMs; the layout keeps every output with one owner).
+// take one half of the row's 128 columns each), warp 8 issues the TMA copies (rings of 3 and 2
+// tiles for the two walked operands), warp 9 issues the MMAs from one thread, warp 10 waits on
+// the copies for it. The MMA warp learns of every event through hardware named barriers (see
+// kBwdBarP1 below); every other wait is an mbarrier wait with a time limit. The two 128-column
+// score regions swap roles every block, so the next block's scores go into the region phase 2
+// has just consumed while this block's gradient GEMMs run, and phase 1 of the next block
+// overlaps them (recomputing S and dP in the dQ kernel costs 2 of its 3 GEMMs; the layout keeps
+// every output with one owner).
 //
 // P is rounded to bf16 for dV = P^T dO and dS to bf16 for the two gradient GEMMs; all
 // accumulation is fp32 in TMEM; outputs are rounded once to bf16.
