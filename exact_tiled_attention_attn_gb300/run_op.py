@@ -38,6 +38,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=None)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0, help="rmsnorm: rows T of X[T, 1024] (default: the workload's)")
     args = ap.parse_args(argv)
 
     import torch
@@ -91,6 +92,8 @@ def main(argv=None):
             work, unit = 2 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (E4M3 KV stream)"
     else:
         shp = W.NORM_QWEN
+        if args.rows > 0:
+            shp = W.NormShape(f"RMSNorm X[{args.rows},{shp.D}]", args.rows, shp.D, shp.eps, shp.seed)
         x, w = W.norm_inputs(shp)
         x, w = x.to(dev), w.to(dev)
         y = torch.empty_like(x)
