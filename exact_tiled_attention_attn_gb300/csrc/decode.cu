@@ -43,8 +43,9 @@ struct DecodeCfg {
   static constexpr int kElems = 8 * kChunks;           // row elements per lane
   static constexpr int kTokPerPass = 32 / kLanesPerTok;
   static constexpr int kConsumerWarps = 4;
-  static constexpr int kTile = 64;                     // rows (tokens) per stage: R = 8 rows per lane
-  static constexpr int kStages = 2;                    // group (d = 128) per tile; 3 CTAs per SM
+  static constexpr int kTile = 64;                     // rows (tokens) per stage; at d = 128 each lane
+                                                       // group takes R = 8 of them per stage
+  static constexpr int kStages = 2;                    // two stages per CTA, three CTAs per SM
   static constexpr int kTokPerWarp = kTile / kConsumerWarps;
   static constexpr int kPasses = kTokPerWarp / kTokPerPass;
   static constexpr int kRowBytes = D * EB;
