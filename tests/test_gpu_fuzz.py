@@ -1,0 +1,110 @@
+"""Randomised parity sweep: seeded random shapes for prefill, backward and decode against the
+float64 oracle, at the tolerances of the other parity tests.
+
+The fixed tests pick shapes by hand (tile edges, tails, groupings). Here the shapes are drawn
+from a fixed seed, so that the combinations nobody picked get covered too:
+* batch and head counts, with the query heads a multiple of the K/V heads;
+* Tq != Tk on both sides of each other, including lengths below, at and past a tile;
+* causal and not, d = 64 and 128;
+* decode lengths anywhere in [1, Lcap] and split counts up to Lcap / 16.
+
+The draws are reproducible; a failure names its case.
+"""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_common import assert_attn_close, f64, require_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def attn():
+    return require_gpu()
+
+
+def _attn_cases(n, seed, max_t):
+    rnd = random.Random(seed)
+    for _ in range(n):
+        Hkv = rnd.choice([1, 1, 2, 3])
+        g = rnd.choice([1, 2, 3, 4])
+        B = rnd.choice([1, 1, 2, 3])
+        Tq = rnd.choice([rnd.randint(1, 130), rnd.randint(1, max_t)])
+        Tk = rnd.choice([Tq, rnd.randint(1, max_t)])
+        d = rnd.choice([64, 128])
+        causal = rnd.choice([False, True])
+        yield B, Hkv * g, Hkv, Tq, Tk, d, causal, rnd.randint(0, 10**6)
+
+
+@pytest.mark.parametrize("case", list(_attn_cases(48, 2024, 700)), ids=lambda c: "B{}_Hq{}_Hkv{}_Tq{}_Tk{}_d{}_c{}".format(*c[:7]))
+def test_prefill_random_shapes(attn, case):
+    B, Hq, Hkv, Tq, Tk, d, causal, seed = case
+    q, k, v = W.attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    O, L = oracle.attention(f64(q), f64(k), f64(v), causal, scale)
+    assert_attn_close(o, lse, O, L, f"prefill {case[:7]}")
+
+
+def _grad_close(got, want, what):
+    got = f64(got)
+    err = np.abs(got - want)
+    scale_max, scale_mean = np.abs(want).max(), np.abs(want).mean()
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert err.max() <= 2e-2 * scale_max + 1e-6, f"{what}: max err {err.max():.3e} vs max |ref| {scale_max:.3e}"
+    assert err.mean() <= 1e-2 * scale_mean + 1e-7, f"{what}: mean err {err.mean():.3e} vs mean |ref| {scale_mean:.3e}"
+
+
+@pytest.mark.parametrize("case", list(_attn_cases(32, 4048, 400)), ids=lambda c: "B{}_Hq{}_Hkv{}_Tq{}_Tk{}_d{}_c{}".format(*c[:7]))
+def test_backward_random_shapes(attn, case):
+    B, Hq, Hkv, Tq, Tk, d, causal, seed = case
+    q, k, v = W.attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed)
+    do = W.grad_output(B, Hq, Tq, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, lse = attn.fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = attn.bwd(qd, kd, vd, o, lse, do.to(DEV), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    O, L = oracle.attention(qf, kf, vf, causal, scale)
+    dQ, dK, dV = oracle.attention_backward(qf, kf, vf, O, L, f64(do), causal, scale)
+    tag = f"backward {case[:7]}"
+    _grad_close(dq, dQ, "dQ " + tag)
+    _grad_close(dk, dK, "dK " + tag)
+    _grad_close(dv, dV, "dV " + tag)
+
+
+def _decode_cases(n, seed):
+    rnd = random.Random(seed)
+    for _ in range(n):
+        Hkv = rnd.choice([1, 2, 4, 8])
+        g = rnd.choice([1, 2, 3, 4, 6])
+        B = rnd.randint(1, 6)
+        Lcap = rnd.choice([rnd.randint(1, 64), rnd.randint(16, 3000)])
+        lens = [rnd.randint(1, Lcap) for _ in range(B)]
+        d = rnd.choice([64, 128])
+        smax = max(1, (Lcap + 15) // 16)
+        S = rnd.randint(1, min(smax, 64))
+        yield B, Hkv * g, Hkv, d, Lcap, tuple(lens), S, rnd.randint(0, 10**6)
+
+
+@pytest.mark.parametrize("case", list(_decode_cases(48, 8096)), ids=lambda c: "B{}_Hq{}_Hkv{}_d{}_L{}_S{}".format(c[0], c[1], c[2], c[3], c[4], c[6]))
+def test_decode_random_shapes(attn, case):
+    B, Hq, Hkv, d, Lcap, lens, S, seed = case
+    shp = W.DecodeShape("fuzz", B, Hq, Hkv, d, 1, Lcap, seed)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=list(lens))
+    o, lse = attn.decode(q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV), num_splits=S)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    O, L = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), shp.scale)
+    assert_attn_close(o, lse, O, L, f"decode {case[:7]}")
