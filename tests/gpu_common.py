@@ -31,6 +31,12 @@ def f64(t):
     return t.detach().to("cpu").to(torch.float64).numpy()
 
 
+def bf16_round(v):
+    """Round-to-nearest-even to bf16 of float64 values (8 significant bits), from frexp."""
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
 def assert_attn_close(o, lse, O, L, what=""):
     o = f64(o) if isinstance(o, torch.Tensor) else o
     err = np.abs(o - O)

@@ -6,7 +6,10 @@ from a fixed seed, so that the combinations nobody picked get covered too:
 * batch and head counts, with the query heads a multiple of the K/V heads;
 * Tq != Tk on both sides of each other, including lengths below, at and past a tile;
 * causal and not, d = 64 and 128;
-* decode lengths anywhere in [1, Lcap] and split counts up to Lcap / 16.
+* decode lengths anywhere in [1, Lcap] and split counts up to Lcap / 16, for the bf16 and the
+  E4M3 cache;
+* RMSNorm rows and widths on both sides of the block-per-row threshold, with and without the
+  residual add.
 
 The draws are reproducible; a failure names its case.
 """
@@ -19,7 +22,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import assert_attn_close, f64, require_gpu
+from gpu_common import assert_attn_close, assert_norm_close, bf16_round, f64, require_gpu
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -108,3 +111,51 @@ def test_decode_random_shapes(attn, case):
     assert attn.last_device_error() == 0
     O, L = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), shp.scale)
     assert_attn_close(o, lse, O, L, f"decode {case[:7]}")
+
+
+@pytest.mark.parametrize("case", list(_decode_cases(24, 16192)), ids=lambda c: "B{}_Hq{}_Hkv{}_d{}_L{}_S{}".format(c[0], c[1], c[2], c[3], c[4], c[6]))
+def test_decode_fp8_random_shapes(attn, case):
+    # the cache quantised on the GPU (codes byte-exact with the oracle's, tested elsewhere), then
+    # decoded; the oracle decodes its own codes and scales
+    B, Hq, Hkv, d, Lcap, lens, S, seed = case
+    shp = W.DecodeShape("fuzz", B, Hq, Hkv, d, 1, Lcap, seed)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=list(lens))
+    kcodes, ksc = attn.kv_quantize_fp8(kc.to(DEV))
+    vcodes, vsc = attn.kv_quantize_fp8(vc.to(DEV))
+    o, lse = attn.decode_fp8(q.to(DEV), kcodes, vcodes, ksc, vsc, sl.to(DEV), num_splits=S)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    okc, oks = oracle.quantize_kv(f64(kc))
+    ovc, ovs = oracle.quantize_kv(f64(vc))
+    O, L = oracle.decode_fp8(f64(q), okc, ovc, oks, ovs, sl.numpy(), shp.scale)
+    assert_attn_close(o, lse, O, L, f"fp8 decode {case[:7]}")
+
+
+def _norm_cases(n, seed):
+    rnd = random.Random(seed)
+    for _ in range(n):
+        if rnd.random() < 0.5:
+            D = 64 * rnd.randint(1, 128)             # 8 segments, up to 8192
+        else:
+            D = 8 * rnd.randint(1, 512)              # any multiple of 8 up to 4096
+        T = rnd.choice([rnd.randint(1, 8), rnd.randint(1, 600), rnd.randint(500, 3000)])
+        yield T, D, rnd.random() < 0.5, rnd.randint(0, 10**6)
+
+
+@pytest.mark.parametrize("case", list(_norm_cases(32, 32384)), ids=lambda c: "T{}_D{}_res{}".format(*c[:3]))
+def test_rmsnorm_random_shapes(attn, case):
+    T, D, residual, seed = case
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, D, generator=gen).to(torch.bfloat16)
+    w = (0.5 + torch.rand(D, generator=gen)).to(torch.bfloat16)
+    if residual:
+        r = torch.randn(T, D, generator=gen).to(torch.bfloat16)
+        y, h = attn.rmsnorm_residual(x.to(DEV), r.to(DEV), w.to(DEV), eps=1e-6)
+        torch.cuda.synchronize()
+        # h is the exact sum rounded once to bf16; y normalises that stored h
+        assert np.array_equal(f64(h), bf16_round(f64(x) + f64(r))), f"h T{T} D{D}"
+        assert_norm_close(y, oracle.rmsnorm(f64(h), f64(w), 1e-6), f"residual T{T} D{D}")
+    else:
+        y = attn.rmsnorm(x.to(DEV), w.to(DEV), eps=1e-6)
+        torch.cuda.synchronize()
+        assert_norm_close(y, oracle.rmsnorm(f64(x), f64(w), 1e-6), f"T{T} D{D}")

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_common import assert_attn_close, assert_norm_close, f64, require_gpu
+from gpu_common import assert_attn_close, assert_norm_close, bf16_round, f64, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -403,12 +403,6 @@ def test_rmsnorm_batch_invariant(attn, D):
     assert_norm_close(full, oracle.rmsnorm(f64(x), f64(w), 1e-6), f"D{D}")
 
 
-def _bf16_round(v):
-    # round-to-nearest-even to bf16 of float64 values (8 significant bits), from frexp
-    m, e = np.frexp(v)
-    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
-
-
 @pytest.mark.parametrize("T,D", [(1, 4096), (7, 1024), (600, 1024), (4096, 1024), (33, 8192), (300, 1000)])
 def test_rmsnorm_residual(attn, T, D):
     gen = torch.Generator().manual_seed(80 + T + D)
@@ -419,7 +413,7 @@ def test_rmsnorm_residual(attn, T, D):
     torch.cuda.synchronize()
     Y, H = oracle.rmsnorm_residual(f64(x), f64(r), f64(w), 1e-6)
     # h is the exact sum rounded once to bf16
-    assert np.array_equal(f64(h), _bf16_round(H))
+    assert np.array_equal(f64(h), bf16_round(H))
     assert_norm_close(y, Y, f"residual T{T} D{D}")
     # in place: h written over r gives the same y and h
     rd = r.to(DEV)
