@@ -149,3 +149,28 @@ def test_prefill_long_sequences_wrap_the_rings(attn, d, causal, Hq, Hkv, T):
     assert attn.last_device_error() == 0
     O, L = oracle.attention(f64(q), f64(k), f64(v), causal, scale)
     assert_attn_close(o, lse, O, L, f"T{T} d{d} Hq{Hq} Hkv{Hkv} causal{causal}")
+
+
+def test_prefill_long_context_sampled(attn):
+    # one sequence of 65 536 tokens (causal GQA, d = 128): rows near the end accumulate 512 key blocks
+    B, Hq, Hkv, T, d = 1, 4, 1, 65536, 128
+    q, k, v = W.attention_inputs_custom(B, Hq, Hkv, T, T, d, 4242)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    o, lse = o.cpu(), lse.cpu()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    _check_sampled(q, k, v, o, lse, True, scale, [(0, 0), (0, 3)], 4242)
+
+
+def test_decode_long_context(attn):
+    # caches of 131 072 tokens, one sequence full and one not
+    shp = W.DecodeShape("long", 2, 8, 2, 128, 1, 131072, 4343)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=[131072, 100001])
+    S = attn.default_splits(shp.B, shp.Hkv, shp.Lcap)
+    o, lse = attn.decode(q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV), num_splits=S)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    O, L = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), shp.scale)
+    assert_attn_close(o, lse, O, L, f"decode long context, {S} splits")
