@@ -14,20 +14,20 @@
 //   bwd_dkdv_kernel    one CTA per (block of 128 keys, K/V head): walks the g query heads x
 //                      the visible query blocks; per block S^T = K Q^T and dP^T = V dO^T into
 //                      TMEM, 8 warps (two per key row) form P^T (phase 1, from S^T alone) and
-//                      dS^T (phase 2, with dP^T) as bf16 pairs inside S^T's columns, then
-//                      dV += P^T dO and dK += dS^T Q with the A operand from TMEM; dV and dK
-//                      stay in TMEM until the end.
+//                      dS^T (phase 2, with dP^T) as bf16 pairs, each in place over the fp32
+//                      values it came from, then dV += P^T dO and dK += dS^T Q with the A
+//                      operand from TMEM; dV and dK stay in TMEM until the end.
 //   bwd_dq_kernel      one CTA per (block of 128 queries, query head): walks the visible key
 //                      blocks; S = Q K^T, dP = dO V^T, dS (bf16) into S's columns, dQ += dS K.
 // Each kernel: warps 0-7 compute (warps w and w + 4 share TMEM lanes 32(w mod 4) .. + 31 and
 // take one half of the row's 128 columns each), warp 8 issues the TMA copies (rings of 3 and 2
 // tiles for the two walked operands), warp 9 issues the MMAs from one thread, warp 10 waits on
 // the copies for it. The MMA warp learns of every event through hardware named barriers (see
-// kBwdBarP1 below); every other wait is an mbarrier wait with a time limit. The two 128-column
-// score regions swap roles every block, so the next block's scores go into the region phase 2
-// has just consumed while this block's gradient GEMMs run, and phase 1 of the next block
-// overlaps them (recomputing S and dP in the dQ kernel costs 2 of its 3 GEMMs; the layout keeps
-// every output with one owner).
+// kBwdBarP1 below); every other wait is an mbarrier wait with a time limit. The next block's
+// scores are issued while this block's gradient GEMMs are still queued, so the compute phases of
+// one block overlap the tensor work of its neighbours (recomputing S and dP in the dQ kernel
+// costs 2 of its 3 GEMMs; the layout keeps every output with one owner). Both grids are numbered
+// longest CTA first.
 //
 // P is rounded to bf16 for dV = P^T dO and dS to bf16 for the two gradient GEMMs; all
 // accumulation is fp32 in TMEM; outputs are rounded once to bf16.
@@ -65,8 +65,8 @@ struct BwdCfg {
   static constexpr uint32_t kIdescS = make_idesc_bf16_f32(128, 128, false);
   // [128 x D] += A (TMEM, 128 x 128 bf16) . B (128 x D, MN-major)
   static constexpr uint32_t kIdescAcc = make_idesc_bf16_f32(128, D, true);
-  // dK/dV kernel TMEM columns: two 128-column score regions [0, 128) and [128, 256) that swap roles
-  // every block, then the fp32 accumulators dV and dK
+  // dK/dV kernel TMEM columns: region S [0, 128) (S^T, then P^T), region dP [128, 256) (dP^T, then
+  // dS^T), then the fp32 accumulators dV and dK
   static constexpr uint32_t kTmAcc0 = 256, kTmAcc1 = 256 + D;
   // dQ kernel TMEM: S in [0, 128) and [128, 256) by turns, dP in [256, 384), the fp32 dQ
   // accumulator from 384
@@ -196,8 +196,13 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
-  const int j0 = blockIdx.x * 128;
+  // Longest CTAs first: the key block is the slow index of the linear CTA number. Under the causal
+  // mask key block kb meets n_qb - kb query blocks, so the CTAs of key block 0 (of every head) start
+  // in the first wave and the short ones fill the tail.
+  const int lin = blockIdx.x + gridDim.x * blockIdx.y;
+  const int bh = lin % gridDim.y, kb = lin / gridDim.y;
+  const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+  const int j0 = kb * 128;
   const int n_qb = (p.Tq + 127) / 128;
   // query blocks that see any key of this block (top-left causal: query q sees key j iff j <= q)
   const int i_first = p.causal ? j0 / 128 : 0;
@@ -278,13 +283,13 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer (the whole warp runs the loop for the named barriers; lane 0 issues) ----------------
-    // The two 128-column score regions swap roles every block: S^T(i) goes to region i & 1 and
-    // dP^T(i) to the other one. The compute warps turn S^T(i) into P^T(i) (phase 1, needs only
-    // S^T) and then, with dP^T(i), into dS^T(i) (phase 2), both kept inside S^T(i)'s region, so
-    // dP^T(i)'s region is free once phase 2 is done: S^T(i + 1) goes there while dV(i), dK(i)
-    // read P^T(i), dS^T(i), and dP^T(i + 1) follows into S^T(i)'s region (the tensor pipe runs
-    // one thread's MMAs in issue order). Phase 1 of block i + 1 overlaps dK(i) and dP^T(i + 1),
-    // and dV(i) (which needs only P^T) is issued once phase 1 is done, overlapping phase 2.
+    // Region S holds S^T(i), which phase 1 turns into P^T(i) in place; region dP holds dP^T(i),
+    // which phase 2 turns into dS^T(i) in place. Per block the issue order is
+    //   [P1] dV(i) | S^T(i + 1) | [P] dK(i) | dP^T(i + 1)
+    // The tensor pipe runs one thread's MMAs in issue order, so S^T(i + 1) overwrites P^T(i) only
+    // after dV(i) has read it, and dP^T(i + 1) overwrites dS^T(i) only after dK(i). S^T(i + 1)
+    // does not wait for phase 2 of block i, and phase 1 of block i + 1 runs while dK(i) and
+    // dP^T(i + 1) occupy the pipe.
     const uint64_t aK = make_sdesc_sw128(smem_u32(sK), 16, 1024), aV = make_sdesc_sw128(smem_u32(sV), 16, 1024);
     // descriptors of the streamed tiles: Q(i) at tile 2 + i mod 3, dO(i) at 5 + i mod 2; K-major for the
     // score GEMMs, MN-major (LBO one box) as the B operand of dV and dK
@@ -297,45 +302,49 @@ __global__ void __launch_bounds__(352, 1)
     // K, V and the first Q, dO tiles: the issuing thread's own waits, once per CTA. After a failed
     // wait (or an abort) the handoffs below still run to the end; only the MMAs are skipped.
     bool ok = true;
+    // region S (columns [0, 128)) holds S^T, then P^T; region dP ([128, 256)) holds dP^T, then dS^T
+    const uint32_t r_s = tmem, r_d = tmem + 128;
     if (lane == 0 && n_it > 0) {
       ok = mbar_wait(&kv_full, 0, abort_p, kBwdWaitTimeoutNs) && mbar_wait(&q_full[0], 0, abort_p, kBwdWaitTimeoutNs) &&
            mbar_wait(&do_full[0], 0, abort_p, kBwdWaitTimeoutNs);
       if (ok) {
         tc_fence_after();
-        bwd_mma_scores<D>(tmem, aK, aQ_of(0));  // S^T(0) = K Q^T into region 0
+        bwd_mma_scores<D>(r_s, aK, aQ_of(0));   // S^T(0) = K Q^T
         umma_commit(&s_ready);
+        bwd_mma_scores<D>(r_d, aV, aDO_of(0));  // dP^T(0) = V dO^T
+        umma_commit(&dp_ready);
       }
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     for (int it = 0; it < n_it; ++it) {
-      const uint32_t r_s = tmem + (it & 1) * 128, r_d = tmem + ((it + 1) & 1) * 128;
-      if (lane == 0 && ok) {
-        bwd_mma_scores<D>(r_d, aV, aDO_of(it));  // dP^T(i) = V dO^T
-        umma_commit(&dp_ready);
-      }
-      // dV needs only P^T: it runs while phase 2 forms dS^T in the other columns of the region
       __syncwarp();
-      named_bar_sync(kBwdBarP1, kBwdComputeAndMma);
+      named_bar_sync(kBwdBarP1, kBwdComputeAndMma);  // P^T(i) is in region S
       if (lane == 0 && ok) {
         tc_fence_after();
         bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc0, r_s, 0, bDO_of(it), it > 0);   // dV += P^T dO
         umma_commit(&do_empty[it & 1]);  // dO(i) read for the last time
       }
-      __syncwarp();
-      named_bar_sync(kBwdBarP, kBwdComputeAndMma);
-      if (it + 1 < n_it) {  // S^T(i + 1) into dP^T(i)'s region, which phase 2 has consumed
+      if (it + 1 < n_it) {
+        // S^T(i + 1) overwrites P^T(i) after dV(i) has read it (MMAs run in issue order), while
+        // phase 2 of block i still works in region dP: phase 1 of the next block starts early
         named_bar_sync(kBwdBarGo, kBwdPair);     // Q(i + 1) and dO(i + 1) are in shared memory
         named_bar_arrive(kBwdBarAck, kBwdPair);
         if (lane == 0 && ok) {
           tc_fence_after();
-          bwd_mma_scores<D>(r_d, aK, aQ_of(it + 1));
+          bwd_mma_scores<D>(r_s, aK, aQ_of(it + 1));
           umma_commit(&s_ready);
         }
       }
+      __syncwarp();
+      named_bar_sync(kBwdBarP, kBwdComputeAndMma);  // dS^T(i) is in region dP
       if (lane == 0 && ok) {
         tc_fence_after();
-        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_s, 32, bQ_of(it), it > 0);   // dK += dS^T Q
+        bwd_mma_accumulate_split<D>(tmem + Cfg::kTmAcc1, r_d, 0, bQ_of(it), it > 0);   // dK += dS^T Q
         umma_commit(&q_empty[it % 3]);  // Q(i) read for the last time
+        if (it + 1 < n_it) {
+          bwd_mma_scores<D>(r_d, aV, aDO_of(it + 1));  // dP^T(i + 1) over dS^T(i), after dK(i) has read it
+          umma_commit(&dp_ready);
+        }
       }
     }
     if (lane == 0) umma_commit(&acc_done);  // every MMA issued above has completed when this arrives
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(352, 1)
         else ndl_s[row] = q < p.Tq ? -p.delta[r] : 0.f;
       }
       named_bar_sync(1, 256);
-      const uint32_t r_s = tmem + lane_off + (it & 1) * 128, r_d = tmem + lane_off + ((it + 1) & 1) * 128;
+      const uint32_t r_s = tmem + lane_off, r_d = tmem + lane_off + 128;
       float pv[64];  // this thread's 64 probabilities, kept between the two phases
       if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&s_ready, static_cast<uint32_t>(it) & 1u, abort_p,
                                                       kBwdWaitTimeoutNs));
@@ -407,8 +416,8 @@ __global__ void __launch_bounds__(352, 1)
                                                       kBwdWaitTimeoutNs));
       if (ok) {
         tc_fence_after();
-        // phase 2: dS^T = P^T (dP^T - D) into [64 half + 32 + 16 cc, + 16) of S^T's region (S^T
-        // values there were consumed in phase 1); dP^T's region is then free
+        // phase 2: dS^T = P^T (dP^T - D), in place: chunk cc reads dP^T columns [64 half + 32 cc, + 32)
+        // and writes its bf16 pairs to [64 half + 16 cc, + 16), inside what this half has read
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int q0 = half * 64 + cc * 32;
@@ -427,7 +436,7 @@ __global__ void __launch_bounds__(352, 1)
             dd[2 * v4] = pack_bf16x2(g01.x, g01.y);
             dd[2 * v4 + 1] = pack_bf16x2(g23.x, g23.y);
           }
-          tmem_st16(r_s + half * 64 + 32 + cc * 16, dd);
+          tmem_st16(r_d + half * 64 + cc * 16, dd);
         }
         tmem_st_wait();
       }
@@ -471,9 +480,14 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
+  // Longest CTAs first: the query block is the slow index of the linear CTA number, counted down
+  // under the causal mask, where query block qb meets qb + 1 key blocks.
+  const int lin = blockIdx.x + gridDim.x * blockIdx.y;
+  const int bh = lin % gridDim.y, slot = lin / gridDim.y;
+  const int qb = p.causal ? static_cast<int>(gridDim.x) - 1 - slot : slot;
+  const int b = bh / p.Hq, h = bh % p.Hq;
   const int kvh = h / p.g;
-  const int i0 = blockIdx.x * 128;
+  const int i0 = qb * 128;
   const int n_kb = (p.Tk + 127) / 128;
   const int last_row = min(i0 + 127, p.Tq - 1);
   const int n_j = p.causal ? min(n_kb, last_row / 128 + 1) : n_kb;

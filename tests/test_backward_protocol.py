@@ -129,15 +129,17 @@ def _run(agents, copies, mma_queue, on_mma, rnd, max_steps):
     raise AssertionError(f"deadlock: no progress; waits per agent: {stuck}")
 
 
-def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_steps=400000):
+def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_steps=400000, compute_warps=8,
+                   early=None):
     rnd = random.Random(seed)
     kv_full = _MBar("kv_full")
     q_full, q_empty = [_MBar(f"q_full[{i}]") for i in range(3)], [_MBar(f"q_empty[{i}]") for i in range(3)]
     do_full, do_empty = [_MBar(f"do_full[{i}]") for i in range(2)], [_MBar(f"do_empty[{i}]") for i in range(2)]
     s_ready, dp_ready, acc_done = _MBar("s_ready"), _MBar("dp_ready"), _MBar("acc_done")
-    p1, pb = _NamedBar("P1", 288), _NamedBar("P", 288)
+    issuer_w, helper_w = compute_warps + 1, compute_warps + 2   # warp compute_warps is the TMA producer
+    p1, pb = _NamedBar("P1", 32 * (compute_warps + 1)), _NamedBar("P", 32 * (compute_warps + 1))
     go, ackb = _NamedBar("Go", 64), _NamedBar("Ack", 64)
-    cbar = _NamedBar("compute", 256)
+    cbar = _NamedBar("compute", 32 * compute_warps)
     copies, mma = [], []
     reads = {}                      # (tile kind, block) -> MMAs still to read it
     q_stage, do_stage = [None] * 3, [None] * 2
@@ -172,10 +174,16 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
             if helper_wait:
                 yield ("m", q_full[k % 3], k // 3)
                 yield ("m", do_full[k & 1], k >> 1)
-            go.arrive(10)
+            go.arrive(helper_w)
             if ack:
-                yield ("n", ackb, ackb.sync(10))
+                yield ("n", ackb, ackb.sync(helper_w))
             yield None
+
+    # TMEM: region S holds S^T(i), then P^T(i); region dP holds dP^T(i), then dS^T(i). Each compute
+    # warp rewrites its own part of a region (its 32 lanes, its half of the columns), so the model
+    # keeps one entry per (region, warp). An MMA writes or reads every part; a phase checks its own
+    # part at its start and at its end, so a write that lands while a phase works is caught.
+    tmem = {(r, w): None for r in ("S", "dP") for w in range(compute_warps)}
 
     def issuer():
         if n_it == 0:
@@ -184,41 +192,74 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
         yield ("m", kv_full, 0)
         yield ("m", q_full[0], 0)
         yield ("m", do_full[0], 0)
-        mma.append(("read", ("q", 0)))
+        mma.append(("read", ("q", 0)))                  # S^T(0)
+        mma.append(("twrite", "S", ("S", 0)))
         mma.append(("commit", s_ready))
+        mma.append(("read", ("do", 0)))                 # dP^T(0)
+        mma.append(("twrite", "dP", ("dP", 0)))
+        mma.append(("commit", dp_ready))
         for it in range(n_it):
-            mma.append(("read", ("do", it)))            # dP^T(i)
-            mma.append(("commit", dp_ready))
-            yield ("n", p1, p1.sync(9))
+            if early != "s":
+                yield ("n", p1, p1.sync(issuer_w))
             mma.append(("read", ("do", it)))            # dV(i)
+            mma.append(("tread", "S", ("P", it)))
             mma.append(("commit", do_empty[it & 1]))
-            yield ("n", pb, pb.sync(9))
             if it + 1 < n_it:
-                yield ("n", go, go.sync(9))
+                yield ("n", go, go.sync(issuer_w))
                 if ack:
-                    ackb.arrive(9)
+                    ackb.arrive(issuer_w)
                 mma.append(("read", ("q", it + 1)))     # S^T(i + 1)
+                mma.append(("twrite", "S", ("S", it + 1)))
                 mma.append(("commit", s_ready))
+            if early == "s":
+                yield ("n", p1, p1.sync(issuer_w))
+            if early != "dp":
+                yield ("n", pb, pb.sync(issuer_w))
             mma.append(("read", ("q", it)))             # dK(i)
+            mma.append(("tread", "dP", ("dS", it)))
             mma.append(("commit", q_empty[it % 3]))
+            if early == "dp":
+                yield ("n", pb, pb.sync(issuer_w))
+            if it + 1 < n_it:
+                mma.append(("read", ("do", it + 1)))    # dP^T(i + 1)
+                mma.append(("twrite", "dP", ("dP", it + 1)))
+                mma.append(("commit", dp_ready))
         mma.append(("commit", acc_done))
+
+    def phase(w, region, want, result):
+        if tmem[region, w] != want:
+            raise AssertionError(f"warp {w} found {tmem[region, w]} in region {region}, wanted {want}")
+        yield None
+        if tmem[region, w] != want:
+            raise AssertionError(f"region {region} overwritten while warp {w} worked on {want}")
+        tmem[region, w] = result
 
     def compute(w):
         for it in range(n_it):
             yield ("n", cbar, cbar.sync(w))
             yield ("n", cbar, cbar.sync(w))
             yield ("m", s_ready, it)
+            yield from phase(w, "S", ("S", it), ("P", it))
             p1.arrive(w)
             yield ("m", dp_ready, it)
+            yield from phase(w, "dP", ("dP", it), ("dS", it))
             pb.arrive(w)
             yield None
         if n_it > 0:
             yield ("m", acc_done, 0)
 
     def on_mma(op):
-        kind, arg = op
+        kind, arg = op[0], op[1]
         if kind == "commit":
             arg.arrive()
+        elif kind == "twrite":
+            for w in range(compute_warps):
+                tmem[arg, w] = op[2]
+        elif kind == "tread":
+            for w in range(compute_warps):
+                if tmem[arg, w] != op[2]:
+                    raise AssertionError(f"an MMA read {tmem[arg, w]} from warp {w}'s part of region {arg}, "
+                                         f"wanted {op[2]}")
         else:
             which, j = arg
             landed = (j // 3) in q_full[j % 3].done if which == "q" else (j >> 1) in do_full[j & 1].done
@@ -226,7 +267,7 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
                 raise AssertionError(f"an MMA read {which}({j}) before its copy landed")
             reads[arg] -= 1
 
-    agents = [producer(), helper(), issuer()] + [compute(w) for w in range(8)]
+    agents = [producer(), helper(), issuer()] + [compute(w) for w in range(compute_warps)]
     _run(agents, copies, mma, on_mma, rnd, max_steps)
 
 
@@ -371,3 +412,10 @@ def test_model_catches_a_missing_ack():
     # without the acknowledgement the helper can arrive on Go twice before the MMA warp syncs
     assert any(_fails(_simulate_dkdv, n_it=9, seed=s, ack=False) for s in range(30)) or \
         any(_fails(_simulate_dq, n_j=9, seed=s, ack=False) for s in range(30))
+
+
+@pytest.mark.parametrize("early", ["s", "dp"])
+def test_model_catches_a_region_overwritten_early(early):
+    # S^T(i + 1) issued before phase 1 of block i has turned S^T(i) into P^T(i), or dK(i) and
+    # dP^T(i + 1) issued before phase 2 has turned dP^T(i) into dS^T(i): the region tracking fails
+    assert any(_fails(_simulate_dkdv, n_it=6, seed=s, early=early) for s in range(30))
