@@ -27,7 +27,7 @@
 // scores are issued while this block's gradient GEMMs are still queued, so the compute phases of
 // one block overlap the tensor work of its neighbours (recomputing S and dP in the dQ kernel
 // costs 2 of its 3 GEMMs; the layout keeps every output with one owner). Both grids are numbered
-// longest CTA first.
+// longest CTA first within groups of heads (bwd_cta_order).
 //
 // P is rounded to bf16 for dV = P^T dO and dS to bf16 for the two gradient GEMMs; all
 // accumulation is fp32 in TMEM; outputs are rounded once to bf16.
@@ -51,6 +51,23 @@ constexpr uint64_t kBwdWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint32_t kBwdBarP1 = 2, kBwdBarP = 3, kBwdBarGo = 4, kBwdBarAck = 5;
 constexpr uint32_t kBwdComputeAndMma = 288, kBwdPair = 64;
 constexpr float kLog2e = 1.4426950408889634f;
+// CTA order of both kernels: the (batch, head) rows of the grid go in groups of this many, and
+// within a group the longest CTAs come first. The group bounds the data that the running CTAs
+// share through L2 (in the dK/dV kernel, a row's Q and dO: 67 MB for 4 rows of the causal GQA
+// prefill workload, B2 Hq32 Hkv8 T8192 d128); longest-first keeps the last CTAs short. Ordered
+// longest-first over the whole grid at once, the dK/dV kernel read 3.2x its inputs from DRAM.
+constexpr int kBwdOrderGroup = 4;
+
+// Linear CTA number -> (row of the grid in y, position along x), as above: groups of
+// kBwdOrderGroup rows, position-major within a group (the last group may be smaller).
+__device__ __forceinline__ void bwd_cta_order(int& row_y, int& pos_x) {
+  const int lin = blockIdx.x + gridDim.x * blockIdx.y;
+  const int grp = lin / (kBwdOrderGroup * static_cast<int>(gridDim.x));
+  const int gsz = min(kBwdOrderGroup, static_cast<int>(gridDim.y) - grp * kBwdOrderGroup);
+  const int within = lin - grp * kBwdOrderGroup * static_cast<int>(gridDim.x);
+  row_y = grp * kBwdOrderGroup + within % gsz;
+  pos_x = within / gsz;
+}
 
 template <int D>
 struct BwdCfg {
@@ -196,11 +213,10 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Longest CTAs first: the key block is the slow index of the linear CTA number. Under the causal
-  // mask key block kb meets n_qb - kb query blocks, so the CTAs of key block 0 (of every head) start
-  // in the first wave and the short ones fill the tail.
-  const int lin = blockIdx.x + gridDim.x * blockIdx.y;
-  const int bh = lin % gridDim.y, kb = lin / gridDim.y;
+  // Longest CTAs first within each group of (batch, K/V head) rows: under the causal mask key
+  // block kb meets n_qb - kb query blocks, so key block 0 of each head starts first.
+  int bh, kb;
+  bwd_cta_order(bh, kb);
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
   const int j0 = kb * 128;
   const int n_qb = (p.Tq + 127) / 128;
@@ -480,10 +496,10 @@ __global__ void __launch_bounds__(352, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Longest CTAs first: the query block is the slow index of the linear CTA number, counted down
-  // under the causal mask, where query block qb meets qb + 1 key blocks.
-  const int lin = blockIdx.x + gridDim.x * blockIdx.y;
-  const int bh = lin % gridDim.y, slot = lin / gridDim.y;
+  // Longest CTAs first within each group of (batch, query head) rows: under the causal mask query
+  // block qb meets qb + 1 key blocks, so the query blocks are counted down.
+  int bh, slot;
+  bwd_cta_order(bh, slot);
   const int qb = p.causal ? static_cast<int>(gridDim.x) - 1 - slot : slot;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int kvh = h / p.g;
