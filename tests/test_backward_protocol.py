@@ -19,12 +19,19 @@ with copies and MMAs completing asynchronously in order. It checks that:
 * no warp arrives twice on a named barrier within one generation, so no
   arrival runs a generation ahead;
 * no parity wait passes on the wrong phase;
-* no stage is overwritten while an MMA still has to read it;
+* no stage is overwritten while an MMA still has to read it, and no MMA reads
+  a stage before its copy has landed;
+* in the dK/dV kernel, every MMA finds in each compute warp's part of the two
+  TMEM score regions what it reads (S^T, P^T, dP^T or dS^T of the right
+  block), and nothing is written to a part while its warp works on it;
 * the schedule always finishes, with no deadlock (a hang on the GPU).
 
-Taking out the Ack handshake, letting the helper hand a tile over without
-waiting for its copy, or having it hand over the wrong tile, makes it fail. The check also covers MMA reads: no MMA
-may read a stage before its copy has landed.
+Each of these changes makes it fail:
+* taking out the Ack handshake;
+* letting the helper hand a tile over without waiting for its copy;
+* having it hand over the wrong tile;
+* issuing the next block's S^T, or dK and the next dP^T, before the compute
+  phase that frees their region.
 """
 import random
 
