@@ -21,9 +21,10 @@ with copies and MMAs completing asynchronously in order. It checks that:
 * no parity wait passes on the wrong phase;
 * no stage is overwritten while an MMA still has to read it, and no MMA reads
   a stage before its copy has landed;
-* in the dK/dV kernel, every MMA finds in each compute warp's part of the two
-  TMEM score regions what it reads (S^T, P^T, dP^T or dS^T of the right
-  block), and nothing is written to a part while its warp works on it;
+* every MMA finds in each compute warp's part of the TMEM score regions what it
+  reads, and nothing is written to a part while its warp works on it:
+  - dK/dV kernel: S^T, P^T, dP^T or dS^T of the right block;
+  - dQ kernel: S in two alternating regions, dP in a third, dS over S;
 * the schedule always finishes, with no deadlock (a hang on the GPU).
 
 Each of these changes makes it fail:
@@ -31,7 +32,8 @@ Each of these changes makes it fail:
 * letting the helper hand a tile over without waiting for its copy;
 * having it hand over the wrong tile;
 * issuing the next block's S^T, or dK and the next dP^T, before the compute
-  phase that frees their region.
+  phase that frees their region (dK/dV);
+* issuing S(j + 2) before dQ(j), or dP(j + 1) before phase 2 of block j (dQ).
 """
 import random
 
@@ -278,7 +280,7 @@ def _simulate_dkdv(n_it, seed, ack=True, helper_skew=0, helper_wait=True, max_st
     _run(agents, copies, mma, on_mma, rnd, max_steps)
 
 
-def _simulate_dq(n_j, seed, ack=True, helper_wait=True, max_steps=400000):
+def _simulate_dq(n_j, seed, ack=True, helper_wait=True, max_steps=400000, early=None):
     rnd = random.Random(seed)
     qd_full = _MBar("qd_full")
     k_full, k_empty = [_MBar(f"k_full[{i}]") for i in range(3)], [_MBar(f"k_empty[{i}]") for i in range(3)]
@@ -288,6 +290,10 @@ def _simulate_dq(n_j, seed, ack=True, helper_wait=True, max_steps=400000):
     copies, mma = [], []
     reads = {}
     k_stage, v_stage = [None] * 3, [None] * 2
+    # TMEM, one entry per (region, compute warp): S(j) goes to region R(j mod 2) and is read by
+    # phase 1; dP(j) goes to region dP; phase 2 reads dP(j) and writes dS(j) over S(j); dQ(j) reads
+    # dS(j). A phase checks its part at its start and at its end.
+    tmem = {(r, w): None for r in ("R0", "R1", "dP") for w in range(8)}
 
     def producer():
         if n_j == 0:
@@ -317,12 +323,19 @@ def _simulate_dq(n_j, seed, ack=True, helper_wait=True, max_steps=400000):
 
     def issue_s(j):
         mma.append(("read", ("k", j)))
+        mma.append(("twrite", f"R{j & 1}", ("S", j)))
         mma.append(("commit", s_ready[j & 1]))
 
     def issue_dp(j):
         mma.append(("read", ("v", j)))
+        mma.append(("twrite", "dP", ("dP", j)))
         mma.append(("commit", dp_ready))
         mma.append(("commit", v_empty[j & 1]))
+
+    def issue_dq(j):
+        mma.append(("read", ("k", j)))
+        mma.append(("tread", f"R{j & 1}", ("dS", j)))
+        mma.append(("commit", k_empty[j % 3]))
 
     def helper():
         for j in range(n_j):
@@ -351,33 +364,60 @@ def _simulate_dq(n_j, seed, ack=True, helper_wait=True, max_steps=400000):
                 yield ("m", k_full[1], 0)
                 issue_s(1)
         for j in range(n_j):
-            yield ("n", pb, pb.sync(9))
+            if early != "dp":
+                yield ("n", pb, pb.sync(9))
             if j + 1 < n_j:
                 yield ("n", go, go.sync(9))
                 if ack:
                     ackb.arrive(9)
                 issue_dp(j + 1)
-            mma.append(("read", ("k", j)))
-            mma.append(("commit", k_empty[j % 3]))
+            if early == "dp":
+                yield ("n", pb, pb.sync(9))
+            if early != "s":
+                issue_dq(j)
             if j + 2 < n_j:
                 yield ("n", go, go.sync(9))
                 if ack:
                     ackb.arrive(9)
                 issue_s(j + 2)
+            if early == "s":
+                issue_dq(j)
         mma.append(("commit", acc_done))
+
+    def check(w, region, want, what):
+        if tmem[region, w] != want:
+            raise AssertionError(f"warp {w} {what}: found {tmem[region, w]} in region {region}, wanted {want}")
 
     def compute(w):
         for j in range(n_j):
+            r = f"R{j & 1}"
             yield ("m", s_ready[j & 1], j >> 1)
+            check(w, r, ("S", j), "phase 1 start")
+            yield None
+            check(w, r, ("S", j), "phase 1 end")
             yield ("m", dp_ready, j)
+            check(w, "dP", ("dP", j), "phase 2 start")
+            check(w, r, ("S", j), "phase 2 start")
+            yield None
+            check(w, "dP", ("dP", j), "phase 2 end")
+            check(w, r, ("S", j), "phase 2 end")
+            tmem[r, w] = ("dS", j)
             pb.arrive(w)
             yield None
         yield ("m", acc_done, 0)
 
     def on_mma(op):
-        kind, arg = op
+        kind, arg = op[0], op[1]
         if kind == "commit":
             arg.arrive()
+        elif kind == "twrite":
+            for w in range(8):
+                tmem[arg, w] = op[2]
+        elif kind == "tread":
+            for w in range(8):
+                if tmem[arg, w] != op[2]:
+                    raise AssertionError(f"an MMA read {tmem[arg, w]} from warp {w}'s part of region {arg}, "
+                                         f"wanted {op[2]}")
         else:
             which, j = arg
             landed = (j // 3) in k_full[j % 3].done if which == "k" else (j >> 1) in v_full[j & 1].done
@@ -426,3 +466,11 @@ def test_model_catches_a_region_overwritten_early(early):
     # S^T(i + 1) issued before phase 1 of block i has turned S^T(i) into P^T(i), or dK(i) and
     # dP^T(i + 1) issued before phase 2 has turned dP^T(i) into dS^T(i): the region tracking fails
     assert any(_fails(_simulate_dkdv, n_it=6, seed=s, early=early) for s in range(30))
+
+
+@pytest.mark.parametrize("early", ["s", "dp"])
+def test_dq_model_catches_a_region_overwritten_early(early):
+    # S(j + 2) issued before dQ(j) has read dS(j) from the same region, or dP(j + 1) issued before
+    # phase 2 of block j has read dP(j): the region tracking fails
+    assert any(_fails(_simulate_dq, n_j=7, seed=s, early=early) for s in range(30))
+
