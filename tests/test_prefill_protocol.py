@@ -36,7 +36,12 @@ asynchronous completions (copies, MMAs), and checks that no barrier is re-armed
 while its phase is pending, that no parity wait succeeds on the wrong phase,
 that no K/V slot or Q buffer is overwritten while an MMA still has to read it,
 that a unit's first P.V product (which overwrites O_q) comes after the previous
-unit's epilogue read O_q, and that the schedule never deadlocks. The kernel's
+unit's epilogue read O_q, and that the schedule never deadlocks. It also tracks
+what each tile's TMEM regions hold:
+* the softmax of block j must find S_q(j) in S_q, and O_q through block j - 1;
+* P.V(j) must read P_q(j) there;
+* the epilogue must read the final O_q;
+* nothing may change while a phase works on it. The kernel's
 configurations (5 slots for d = 128, 11 for d = 64, R = 8) must pass; a
 too-shallow ring (R = 4 with 11 slots) must fail.
 """
@@ -79,11 +84,13 @@ class _Bar:
         return ready
 
 
-def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=True, counted_tile=1):
+def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=True, counted_tile=1,
+              s_before_pv=False):
     """units: list of (nkv_0, nkv_1) with max >= 1 and nkv_0 >= 1. `counted_tile` is the tile
     whose S-ready signal has its own barrier (one phase per S block of that tile); the other
-    tile waits on iter_done. skip_done_waits=False or counted_tile=0 switch off rules of the
-    kernel's protocol, to show that the model catches their absence."""
+    tile waits on iter_done. skip_done_waits=False, counted_tile=0 or s_before_pv=True (S_q(j)
+    issued ahead of PV_q(j - 1)) switch off rules of the kernel's protocol, to show that the
+    model catches their absence."""
     rnd = random.Random(seed)
     kv_ready = [_Bar(f"kv_ready[{r}]") for r in range(ring)]
     iter_done = [_Bar(f"iter_done[{r}]") for r in range(ring)]
@@ -98,6 +105,9 @@ def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=Tru
     slot_item = [None] * k_slots
     epilogue_done = [-1, -1]   # last unit whose O_q the softmax warps have read
     last_active = [-1, -1]     # last unit in which tile q was active (issuer's view)
+    # TMEM contents per tile: region S_q holds S_q(j) of unit u, which the softmax turns into
+    # P_q(j) in place and PV_q(j) reads; O_q holds the product through block j (PV_q(j) done).
+    tmem = {("S", 0): None, ("S", 1): None, ("O", 0): None, ("O", 1): None}
 
     # reads each item will get: K(j) by S_q(j) for tiles with j < nkv_q, V(j) by PV_q(j) likewise
     item_base = []
@@ -160,19 +170,26 @@ def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=Tru
             for j in range(n + 1):
                 yield (kv_ready[(G + j) % ring], (G + j) // ring)
                 for q, nk in order:
+                    def issue_s():
+                        mma_queue.append(("read", ib + 2 * j))
+                        mma_queue.append(("qread", None))
+                        mma_queue.append(("twrite", (("S", q), ("S", u, j))))
+                        if q == counted_tile:
+                            mma_queue.append(("commit", s_full))
+                    if s_before_pv and j < nk:
+                        issue_s()
                     if j > 0 and j - 1 < nk:
                         yield (p_full[q], pcount[q])
                         pcount[q] += 1
                         if j == 1 and last_active[q] >= 0 and epilogue_done[q] < last_active[q]:
                             raise AssertionError(f"O_{q} overwritten before unit {last_active[q]}'s epilogue")
                         mma_queue.append(("read", ib + 2 * j - 1))
+                        mma_queue.append(("tread", (("S", q), ("P", u, j - 1))))
+                        mma_queue.append(("twrite", (("O", q), ("O", u, j - 1))))
                         if j == nk:
                             mma_queue.append(("commit", o_done[q]))
-                    if j < nk:
-                        mma_queue.append(("read", ib + 2 * j))
-                        mma_queue.append(("qread", None))
-                        if q == counted_tile:
-                            mma_queue.append(("commit", s_full))
+                    if not s_before_pv and j < nk:
+                        issue_s()
                 mma_queue.append(("commit", iter_done[(G + j) % ring]))
                 yield None
             for q, nk in ((0, n0), (1, n1)):
@@ -187,10 +204,23 @@ def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=Tru
             nk = n1 if q else n0
             for j in range(nk):
                 yield (s_full, sc + j) if q == counted_tile else (iter_done[(G + j) % ring], (G + j) // ring)
+                # softmax of block j: reads S_q(j), writes P_q(j) over it, may rescale O_q, whose
+                # product must then run through block j - 1 and stay untouched meanwhile
+                for _ in range(2):
+                    if tmem["S", q] != ("S", u, j):
+                        raise AssertionError(f"softmax {q} found {tmem['S', q]} in S_{q}, wanted S({u}, {j})")
+                    if j > 0 and tmem["O", q] != ("O", u, j - 1):
+                        raise AssertionError(f"softmax {q} found {tmem['O', q]} in O_{q}, wanted O({u}, {j - 1})")
+                    yield None
+                tmem["S", q] = ("P", u, j)
                 p_full[q].arrive()
                 yield None
             if nk > 0:
                 yield (o_done[q], oc)
+                for _ in range(2):   # the epilogue reads the final O_q
+                    if tmem["O", q] != ("O", u, nk - 1):
+                        raise AssertionError(f"epilogue {q} found {tmem['O', q]} in O_{q}, wanted O({u}, {nk - 1})")
+                    yield None
                 epilogue_done[q] = u
                 oc += 1
             sc += nk
@@ -222,6 +252,11 @@ def _simulate(k_slots, ring, units, seed, max_steps=2000000, skip_done_waits=Tru
                 arg.arrive()
             elif kind == "read":
                 reads_left[arg] -= 1
+            elif kind == "twrite":
+                tmem[arg[0]] = arg[1]
+            elif kind == "tread":
+                if tmem[arg[0]] != arg[1]:
+                    raise AssertionError(f"an MMA read {tmem[arg[0]]} from {arg[0]}, wanted {arg[1]}")
             else:
                 q_reads_left[0] -= 1
         live = False
@@ -301,3 +336,11 @@ def test_model_catches_a_missing_protocol_rule():
     seq = [(1, 0), (1, 0), (1, 1), (2, 2), (1, 1), (24, 25)]
     assert not _fails(k_slots=11, ring=8, units=seq, seed=7)
     assert _fails(k_slots=11, ring=8, units=seq, seed=7, skip_done_waits=False, max_steps=200000)
+
+
+def test_model_catches_s_issued_before_the_previous_pv():
+    # S_q(j) issued ahead of PV_q(j - 1) overwrites P_q(j - 1) before the P.V product reads it
+    seq = [(3, 3), (2, 1), (4, 4)]
+    assert not _fails(k_slots=5, ring=8, units=seq, seed=3)
+    assert any(_fails(k_slots=5, ring=8, units=seq, seed=s, s_before_pv=True, max_steps=300000) for s in range(20))
+
