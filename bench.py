@@ -343,6 +343,40 @@ def run_gpu(args):
                           "how": "H2D, attn_fwd, D2H of each step one after another on one stream"}}
         del bufs
 
+    # ---- the other two prefill configurations, each timed on its own outside the step: every
+    #      launch between two events, L2 flushed before it (the causal GQA B1 inputs, 34 MB, fit
+    #      in L2); the median launch is reported
+    prefill_other = {}
+    if not args.no_prefill_configs:
+        flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+        for key, shp in (("prefill_c2", W.MHA_GPT2), ("prefill_c3", W.GQA_QWEN)):
+            pq, pk, pv = [t.to(dev) for t in W.attention_inputs(shp)]
+            po = torch.empty_like(pq)
+            pl = torch.empty(shp.B, shp.Hq, shp.T, dtype=torch.float32, device=dev)
+            for _ in range(3):
+                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl)
+            tms = []
+            for _ in range(20):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl)
+                b.record(stream)
+                torch.cuda.synchronize()
+                tms.append(a.elapsed_time(b))
+            assert attn.last_device_error() == 0
+            tms.sort()
+            p_ms = max_over_ranks([tms[len(tms) // 2]], dev)[0]
+            p_tf = shp.flops() / (p_ms * 1e-3) / 1e12
+            prefill_other[key] = {"value": round(p_tf, 2), "unit": "TFLOP/s", "bound": "tensor",
+                                  "peak": peaks["bf16"], "frac": round(p_tf / peaks["bf16"], 4),
+                                  "ms": round(p_ms, 4), "ms_p10_p90": [round(tms[2], 4), round(tms[-3], 4)],
+                                  "flops_per_launch": shp.flops(), "workload": shp.name,
+                                  "kernel": f"attn_fwd_kernel<{shp.d}>",
+                                  "timing": "median of 20 launches, each between two events, L2 flushed before it"}
+            del pq, pk, pv, po, pl
+        del flush
+
     # ---- RMSNorm at growing T: the workload's 16.8 MB is launch- and latency-bound,
     #      the sweep shows the kernel's sustained bandwidth (L2 flushed before each launch)
     norm_sweep = []
@@ -576,6 +610,8 @@ def run_gpu(args):
                                                   "frac": round(norm_gbs / peaks["hbm"], 4),
                                                   "timing": "one launch between two events inside the step"},
                         "sweep_D1024": norm_sweep},
+            "prefill_c2": prefill_other.get("prefill_c2"),
+            "prefill_c3": prefill_other.get("prefill_c3"),
             "decode_fp8": dec8,
             "rmsnorm_residual": res_line,
             "decode_short_context": short,
@@ -707,6 +743,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV-cache decode line")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass line")
+    ap.add_argument("--no-prefill-configs", action="store_true",
+                    help="skip the lines for the non-causal MHA and the causal GQA B1 prefill configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

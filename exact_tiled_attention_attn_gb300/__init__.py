@@ -21,7 +21,7 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "decode", "decode_noalloc", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
+__all__ = ["fwd", "bwd", "decode", "decode_noalloc", "noalloc_splits", "NOALLOC_SCRATCH_BYTES", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
            "decode_workspace_size",
            "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
@@ -153,35 +153,54 @@ def decode(q, kcache, vcache, seqlens, scale: float | None = None, num_splits: i
     return out, lse
 
 
-def decode_noalloc(q, kcache, vcache, seqlens, scale: float | None = None, num_splits: int | None = None,
-                   out=None, lse=None, return_lse: bool = True, stream=None):
-    """``decode`` without a workspace: the split partials go to the library's fixed
-    32 MiB device array, so the library itself allocates nothing.
+# Size of the library's fixed device array that holds attn_decode_noalloc's split
+# partials (the limit include/attn.h states for that entry point).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
-    For callers that cannot allocate device memory at decode time (a KV-cache pool
-    that owns the memory, an allocation budget, no allocation allowed mid-step).
-    ``out`` and ``lse`` must then be passed in as well. All such calls share the one
-    array: calls that can overlap on the GPU must be serialised by the caller. The
-    first call on a device looks the array up and should come before any stream
-    capture. Raises AttnError (ATTN_ERR_WORKSPACE) when the partials for
-    ``num_splits`` would not fit in 32 MiB.
+
+def noalloc_splits(B: int, Hq: int, Hkv: int, d: int, Lcap: int) -> int:
+    """The default split count, lowered (halved) until the partials fit the fixed array."""
+    s = default_splits(B, Hkv, Lcap)
+    while s > 1 and decode_workspace_size(B, Hq, d, s) > NOALLOC_SCRATCH_BYTES:
+        s //= 2
+    return s
+
+
+def decode_noalloc(q, kcache, vcache, seqlens, out, lse=None, scale: float | None = None,
+                   num_splits: int | None = None, stream=None):
+    """``decode`` without a workspace, for callers that cannot allocate device memory
+    at decode time (a KV-cache pool that owns the memory, an allocation budget, no
+    allocation allowed mid-step). The split partials go to the library's fixed
+    32 MiB device array, and this function allocates nothing either: the caller
+    passes ``out`` [B, Hq, d] bf16 and, if it wants the LSE, ``lse`` [B, Hq] fp32
+    (``lse=None`` skips writing it).
+
+    ``num_splits=None`` takes the default split count, halved until the partials
+    fit in 32 MiB. All such calls share the one array: calls that can overlap on
+    the GPU must be serialised by the caller. The first call on a device looks the
+    array up and should come before any stream capture. Raises AttnError
+    (ATTN_ERR_WORKSPACE) when an explicit ``num_splits`` needs more than 32 MiB.
+    Returns ``(out, lse)``.
     """
     _check_tensor("q", q, torch.bfloat16, 3)
     _check_tensor("kcache", kcache, torch.bfloat16, 4)
     _check_tensor("vcache", vcache, torch.bfloat16, 4)
     _check_tensor("seqlens", seqlens, torch.int32, 1)
+    _check_tensor("out", out, torch.bfloat16, 3)
     B, Hq, d = q.shape
     Hkv, Lcap = kcache.shape[1], kcache.shape[2]
     if kcache.shape != vcache.shape or kcache.shape[0] != B or kcache.shape[3] != d:
         raise ValueError("kcache and vcache must both be [B, Hkv, Lcap, d] matching q")
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, 2)
+        if tuple(lse.shape) != (B, Hq):
+            raise ValueError("lse must be [B, Hq]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if num_splits is None:
-        num_splits = default_splits(B, Hkv, Lcap)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None and return_lse:
-        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        num_splits = noalloc_splits(B, Hq, Hkv, d, Lcap)
     st = _lib.load().attn_decode_noalloc(q.data_ptr(), kcache.data_ptr(), vcache.data_ptr(), seqlens.data_ptr(),
                                          out.data_ptr(), lse.data_ptr() if lse is not None else None,
                                          B, Hq, Hkv, d, Lcap, float(scale), int(num_splits), _stream_ptr(stream))

@@ -19,7 +19,7 @@ cudaError_t launch_rmsnorm(const void* x, const void* r, const void* w, void* y,
                            cudaStream_t s);
 int rmsnorm_segments(int D);
 size_t decode_noalloc_capacity();
-cudaError_t decode_noalloc_scratch(void** ptr);
+cudaError_t decode_noalloc_scratch(cudaStream_t stream, void** ptr);
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Tk,
                             int d, int causal, float scale, void* workspace, cudaStream_t stream, int* launched);
@@ -212,7 +212,7 @@ attn_status attn_decode_noalloc(const void* q, const void* kcache, const void* v
   // The partials must fit the library's fixed scratch; refuse before touching the device.
   if (attn_decode_workspace_size(B, Hq, d, num_splits) > decode_noalloc_capacity()) return ATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (decode_noalloc_scratch(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (decode_noalloc_scratch(stream, &scratch) != cudaSuccess) return ATTN_ERR_CUDA;
   const int C = decode_chunk(Lcap, num_splits);
   int launched = 0;
   const cudaError_t err = launch_decode(q, kcache, vcache, nullptr, nullptr, seqlens, o, lse, B, Hq, Hkv, d, Lcap,

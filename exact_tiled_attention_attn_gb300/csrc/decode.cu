@@ -598,18 +598,24 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeNoAllocSc
 size_t decode_noalloc_capacity() { return kDecodeNoAllocScratchBytes; }
 
 // Device address of g_decode_scratch on the current device. In host code the symbol is
-// only a host-side stand-in, so its device address is looked up once per device (with
-// that device current) and cached. The first lookup on a device may load this library's
-// device code there; it does not call cudaMalloc.
-cudaError_t decode_noalloc_scratch(void** ptr) {
+// only a host-side stand-in, so its device address is looked up with that device current.
+// Outside a stream capture it is looked up on every call (cheap once the module is loaded),
+// so a device reset or a reloaded module never leaves a stale address behind; during a
+// capture the address cached by the last lookup on that device is used, since the first
+// lookup on a device may load this library's device code there. Neither path calls
+// cudaMalloc.
+cudaError_t decode_noalloc_scratch(cudaStream_t stream, void** ptr) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  err = cudaStreamIsCapturing(stream, &cap);
+  if (err != cudaSuccess) return err;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone || addr[dev] == nullptr) {
     void* p = nullptr;
     err = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (err != cudaSuccess) return err;

@@ -9,6 +9,8 @@ mean CUDA-event time of the launches after the first.
   python -m exact_tiled_attention_attn_gb300.run_op --op decode --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op decode_fp8 --iters 3
   python -m exact_tiled_attention_attn_gb300.run_op --op rmsnorm --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op rmsnorm_residual --iters 3
+  python -m exact_tiled_attention_attn_gb300.run_op --op kv_quant --iters 3
 
 Workloads (seeded N(0,1) bf16 inputs):
   single-head  causal 1 x 1 x 256 x 64
@@ -16,7 +18,8 @@ Workloads (seeded N(0,1) bf16 inputs):
   gqa-qwen     causal B1 Hq16 Hkv8 T4096 d128
   gqa-llama    causal B2 Hq32 Hkv8 T8192 d128 (default for prefill)
   decode-llama B16 Hq32 Hkv8 d128, lengths ~U[8192, 32768] (decode)
-  norm-qwen    X[4096, 1024] (rmsnorm)
+  norm-qwen    X[4096, 1024] (rmsnorm, rmsnorm_residual)
+  kv_quant quantises the K cache of decode-llama to E4M3 (one scale per (sequence, head))
 """
 from __future__ import annotations
 
@@ -34,7 +37,8 @@ PREFILL_WORKLOADS = {"single-head": "SINGLE_HEAD", "mha-gpt2": "MHA_GPT2", "gqa-
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["prefill", "backward", "decode", "decode_fp8", "rmsnorm"], required=True)
+    ap.add_argument("--op", choices=["prefill", "backward", "decode", "decode_fp8", "rmsnorm", "rmsnorm_residual",
+                                           "kv_quant"], required=True)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--splits", type=int, default=0)
@@ -90,6 +94,16 @@ def main(argv=None):
             def run():
                 attn.decode_fp8(q, kq, vq, ks, vs, sld, scale=shp.scale, num_splits=S, workspace=ws, out=o, lse=lse)
             work, unit = 2 * shp.Hkv * shp.d * int(sl.sum()) / 1e9, "GB/s (E4M3 KV stream)"
+    elif args.op == "kv_quant":
+        shp = W.DECODE_LLAMA
+        kc = W.decode_inputs(shp)[1].to(dev)
+        codes = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+        sc = torch.empty(shp.B, shp.Hkv, dtype=torch.float32, device=dev)
+
+        def run():
+            attn.kv_quantize_fp8(kc, codes=codes, scale=sc)
+        # the whole bf16 cache is read twice (amax pass, encode pass) and the codes written once
+        work, unit = (2 * kc.numel() * 2 + kc.numel()) / 1e9, "GB/s (2 reads of the bf16 cache + codes)"
     else:
         shp = W.NORM_QWEN
         if args.rows > 0:
@@ -97,10 +111,17 @@ def main(argv=None):
         x, w = W.norm_inputs(shp)
         x, w = x.to(dev), w.to(dev)
         y = torch.empty_like(x)
+        if args.op == "rmsnorm":
+            def run():
+                attn.rmsnorm(x, w, eps=shp.eps, out=y)
+            work, unit = shp.hbm_bytes() / 1e9, "GB/s"
+        else:
+            r = torch.flip(x, dims=[0]).contiguous()
+            h = torch.empty_like(x)
 
-        def run():
-            attn.rmsnorm(x, w, eps=shp.eps, out=y)
-        work, unit = shp.hbm_bytes() / 1e9, "GB/s"
+            def run():
+                attn.rmsnorm_residual(x, r, w, eps=shp.eps, out=y, h=h)
+            work, unit = (8 * shp.T * shp.D + 2 * shp.D) / 1e9, "GB/s"
 
     run()
     torch.cuda.synchronize()

@@ -172,9 +172,12 @@ attn_status attn_decode(const void* q, const void* kcache, const void* vcache,
  *   Size limit: attn_decode_workspace_size(B, Hq, d, num_splits) must be
  *   <= 32 MiB (33554432 bytes); larger requests return ATTN_ERR_WORKSPACE before
  *   anything runs (use fewer splits, or attn_decode with your own workspace).
- *   First call on a device: it looks up the array's device address on the
- *   current device (cudaGetSymbolAddress) and caches it; make that first call
- *   before any stream capture on that device.
+ *   Device address: outside a stream capture every call looks the array's
+ *   address up on the current device (cudaGetSymbolAddress), so a device
+ *   reset or a reloaded module is picked up; inside a capture the address
+ *   found by the last uncaptured call on that device is used. The first call
+ *   on a device may load the library's device code there: make it before any
+ *   stream capture on that device.
  *   Sharing: every call uses the same array, which keeps the previous call's
  *   contents (nothing in it needs to start at zero). Calls that can overlap on
  *   the GPU (other streams, other host threads) race on it: serialise them.

@@ -36,7 +36,7 @@ from .attention import (  # noqa: F401
     attention_backward,
     attention_backward_rows,
 )
-from .rmsnorm import rmsnorm, rmsnorm_rows, rmsnorm_residual  # noqa: F401
+from .rmsnorm import rmsnorm, rmsnorm_residual  # noqa: F401
 from .fp8 import (  # noqa: F401
     E4M3_MAX,
     e4m3_value,

@@ -26,12 +26,6 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)[None, :]
 
 
-def rmsnorm_rows(x: np.ndarray, w: np.ndarray, eps: float, rows) -> np.ndarray:
-    """The same definition evaluated for selected rows only."""
-    rows = np.asarray(rows, dtype=np.int64)
-    return rmsnorm(np.asarray(x)[rows], w, eps)
-
-
 def rmsnorm_residual(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float):
     """x, r: [T, D], w: [D] -> (y, h): h = x + r, y = RMSNorm(h) * w (float64)."""
     h = np.asarray(x, dtype=np.float64) + np.asarray(r, dtype=np.float64)
