@@ -21,7 +21,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgb300attn.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["api.cu", "prefill.cu", "decode.cu", "rmsnorm.cu", "kvquant.cu", "backward.cu", "tmap.cu"]
+SOURCES = ["api.cu", "prefill.cu", "prefill_pair.cu", "decode.cu", "rmsnorm.cu", "kvquant.cu", "backward.cu",
+           "tmap.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                 "-I", os.path.join(ROOT, "include")]

@@ -25,6 +25,7 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
                             int d, int causal, float scale, void* workspace, cudaStream_t stream, int* launched);
 uint32_t backward_take_device_error();
 uint32_t prefill_take_device_error();
+uint32_t prefill_pair_take_device_error();
 uint32_t decode_take_device_error();
 uint32_t rmsnorm_take_device_error();
 
@@ -262,7 +263,8 @@ const char* attn_status_string(attn_status s) {
 
 attn_status attn_last_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  const uint32_t e = prefill_take_device_error() | decode_take_device_error() | rmsnorm_take_device_error() |
+  const uint32_t e = prefill_take_device_error() | prefill_pair_take_device_error() | decode_take_device_error() |
+                     rmsnorm_take_device_error() |
                      backward_take_device_error() | take_device_error_word();
   if (e == 0xFFFFFFFFu) return ATTN_ERR_CUDA;
   if (e & kErrTimeout) return ATTN_ERR_TIMEOUT;

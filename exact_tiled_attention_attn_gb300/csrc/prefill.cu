@@ -35,6 +35,9 @@
 // which finite base is subtracted ("Module 07", section "Online softmax: derivation":
 // the factor exp(m - c) cancels between numerator and denominator), and the bound
 // keeps every p <= 256, far inside fp32 and bf16 range.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace gb300 {
@@ -567,8 +570,19 @@ static cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, co
   return cudaGetLastError();
 }
 
+cudaError_t launch_attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                 int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream);
+
+// Which forward kernel runs: this file's kernel, unless the environment variable
+// GB300_ATTN_PREFILL is "pair" (the CTA-pair kernel of prefill_pair.cu; both compute the same
+// result; the pair kernel is the slower of the two on this part, see prefill_pair.cu).
+static bool use_pair_kernel() {
+  const char* e = std::getenv("GB300_ATTN_PREFILL");
+  return e != nullptr && std::strcmp(e, "pair") == 0;
+}
+
 // Returns cudaErrorInvalidValue if a tensor map cannot be built (e.g. driver entry point missing).
-cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+static cudaError_t launch_attn_fwd_single(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                             int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   if (!encode_bf16_tile_map(&mq, q, d, Tq, B * Hq) || !encode_bf16_tile_map(&mk, k, d, Tk, B * Hkv) ||
@@ -593,6 +607,16 @@ cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o
   if (units <= 0 || units > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
   p.units = static_cast<int>(units);
   return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, stream) : launch_fwd_d<128>(mq, mk, mv, p, stream);
+}
+
+cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+  if (use_pair_kernel()) {
+    const cudaError_t err = launch_attn_fwd_pair(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
+    if (err != cudaErrorInvalidDevice) return err;
+    (void)cudaGetLastError();  // no resident pair on this device: the single-CTA kernel runs
+  }
+  return launch_attn_fwd_single(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
 }
 
 uint32_t prefill_take_device_error() { return take_device_error_word(); }
