@@ -25,7 +25,11 @@
 //
 // Scores are kept in the base-2 domain: q is pre-multiplied by
 // c = scale * log2(e), so p = 2^(c*s - m); LSE = (m + log2 l) * ln 2.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -36,7 +40,8 @@ constexpr float kDecodeRescaleThreshold = 8.0f;           // log2 of the allowed
 constexpr int kDecodeMaxHeadsPerCta = 4;                  // query heads one CTA keeps in registers
 
 // EB = bytes per cached element: 2 for the bf16 cache, 1 for the E4M3 (FP8) cache.
-template <int D, int EB = 2>
+// STAGES = shared-memory stages of K and V per CTA.
+template <int D, int EB = 2, int STAGES = 2>
 struct DecodeCfg {
   static constexpr int kLanesPerTok = D / 8;           // one chunk of 8 elements (8 * EB bytes) per lane
   static constexpr int kChunks = 1;                    // 16-byte chunks per lane per row
@@ -45,7 +50,7 @@ struct DecodeCfg {
   static constexpr int kConsumerWarps = 4;
   static constexpr int kTile = 64;                     // rows (tokens) per stage; at d = 128 each lane
                                                        // group takes R = 8 of them per stage
-  static constexpr int kStages = 2;                    // two stages per CTA, three CTAs per SM
+  static constexpr int kStages = STAGES;               // FFMA kernel: two stages per CTA, three CTAs per SM
   static constexpr int kTokPerWarp = kTile / kConsumerWarps;
   static constexpr int kPasses = kTokPerWarp / kTokPerPass;
   static constexpr int kRowBytes = D * EB;
@@ -422,6 +427,334 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads, 3)
   asm volatile("griddepcontrol.launch_dependents;");
 }
 
+// ---------------------------------------------------------------------------------------
+// Split kernel on warp-level tensor-core MMAs (mma.sync m16n8k16, fp32 accumulation).
+//
+// Same CTA, producer, stages and partial format as decode_split_kernel; the consumers differ.
+// Per element the FFMA kernel above spends ~4 issue slots: its dot products are repeated for
+// every query head of the CTA and a shuffle tree reduces them; with an E4M3 cache each element
+// also needs two conversions. Both products of the step are small dense contractions (the
+// CTA's query heads against 64 keys of d elements), so here each consumer warp takes 16 keys
+// of a stage and runs them through the tensor core:
+//   S = Q K^T   A = Q (16 rows, the CTA's heads in rows 0..nh-1, the rest zero), B = K^T of
+//               8 keys, fp32 accumulators; the d axis is permuted so each thread reads one
+//               contiguous piece of its key row (a dot product does not depend on the order of
+//               its terms, as long as Q and K use the same one);
+//   O += P V    A = P, taken straight from S's accumulator layout (rows = heads, keys 2c,
+//               2c+1 and 8+2c, 8+2c+1 of thread c), B = V of 16 keys x 8 output columns; the
+//               output columns are permuted so each thread reads a contiguous piece of 4 rows.
+// bf16 cache: K and V feed the MMA as they are (bf16 x bf16); P is rounded to bf16, as in the
+// prefill. E4M3 cache: codes become f16 pairs (exact; cvt.rn.f16x2.e4m3x2), q becomes f16
+// (exact for |q| in f16's normal range), P is rounded to f16. Scores leave the MMA unscaled and
+// are multiplied by c = scale * log2(e) (and the keys' dequantisation scale) in fp32.
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[2], const uint32_t a0, const uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+  // rows 8..15 of A are zero, so d2 and d3 stay zero: they are not kept
+  float z2, z3;  // NOLINT: outputs of the instruction, unused
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %10, %10};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void mma_16816_f16(float (&d)[2], const uint32_t a0, const uint32_t a2, uint32_t b0,
+                                              uint32_t b1) {
+  float z2, z3;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %10, %10};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(z2), "=f"(z3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+template <int EB>
+__device__ __forceinline__ void mma_16816(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  if constexpr (EB == 2) mma_16816_bf16(d, a0, a2, b0, b1);
+  else mma_16816_f16(d, a0, a2, b0, b1);
+}
+// two E4M3 codes (bits 0-15 of w, the lower byte first) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(w & 0xFFFFu)));
+  return h2;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Three stages per CTA and two CTAs per SM (the same bytes in flight per SM as the FFMA kernel's
+// two stages and three CTAs; at d = 128 this kernel needs ~168 registers per thread).
+constexpr int kMmaStages = 3;
+constexpr int kMmaCtasPerSm = 2;
+
+template <int D, int EB>
+__global__ void __launch_bounds__(DecodeCfg<D, EB, kMmaStages>::kThreads, kMmaCtasPerSm)
+    decode_split_mma_kernel(const DecodeParams p) {
+  using Cfg = DecodeCfg<D, EB, kMmaStages>;
+  static_assert(Cfg::kTile == 16 * Cfg::kConsumerWarps, "one 16-key block per consumer warp per stage");
+  constexpr int KK = D / 16;          // MMAs along d for S
+  constexpr int NJ = D / 8;           // MMAs along the output columns for O
+  constexpr int QE = D / 4;           // elements of a key row one thread reads for S
+  constexpr int KW = QE * EB / 4;     // 32-bit words of them
+  constexpr int VE = D / 8;           // elements of a value row one thread reads for O
+  constexpr int VW = VE * EB / 4;     // 32-bit words of them
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + Cfg::kStages * Cfg::kTileBytes;
+  __shared__ uint64_t full_bar[Cfg::kStages];
+  __shared__ uint64_t empty_bar[Cfg::kStages];
+  __shared__ int abort_flag;
+
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y / p.n_hblk;
+  const int hb = blockIdx.y % p.n_hblk;
+  const int b = blockIdx.z;
+  const int h0 = kvh * p.g + hb * p.hblk;
+  const int nh = min(p.hblk, (kvh + 1) * p.g - h0);
+  int L = p.seqlens[b];
+  L = L < 0 ? 0 : (L > p.Lcap ? p.Lcap : L);
+  const int start = split * p.C;
+  if (start >= L) return;  // empty split: the combine kernel never reads it
+  const int end = min(start + p.C, L);
+  const int ntiles = (end - start + Cfg::kTile - 1) / Cfg::kTile;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], Cfg::kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abort_p = &abort_flag;
+  const size_t head_off = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Lcap;
+  const uint8_t* kbase = p.kc + head_off * Cfg::kRowBytes;
+  const uint8_t* vbase = p.vc + head_off * Cfg::kRowBytes;
+
+  if (warp == Cfg::kConsumerWarps) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % Cfg::kStages;
+        const uint32_t ph = static_cast<uint32_t>(t / Cfg::kStages) & 1u;
+        if (!mbar_wait(&empty_bar[s], ph ^ 1u, abort_p, kDecodeWaitTimeoutNs)) break;
+        const int row0 = start + t * Cfg::kTile;
+        const int nrows = min(Cfg::kTile, end - row0);
+        const uint32_t bytes = static_cast<uint32_t>(nrows) * Cfg::kRowBytes;
+        mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
+        bulk_copy_g2s(sK + s * Cfg::kTileBytes, kbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes, &full_bar[s]);
+        bulk_copy_g2s(sV + s * Cfg::kTileBytes, vbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes, &full_bar[s]);
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - Cfg::kStages); t < issued; ++t) {
+        const int s = t % Cfg::kStages;
+        mbar_wait(&full_bar[s], static_cast<uint32_t>(t / Cfg::kStages) & 1u, abort_p, kDecodeWaitTimeoutNs);
+      }
+    }
+    __syncwarp();
+    __syncthreads();
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int gq = lane >> 2;  // MMA row group: the query head (rows of A, P, O); the key / column of B
+  const int c = lane & 3;    // position in the group
+  const bool head_ok = gq < nh;
+  // Q as the A operand of S: for MMA kk, this thread's k-slots (2c, 2c+1) and (2c+8, 2c+9) hold
+  // the elements QE c + 4 kk + (0, 1) and QE c + 4 kk + (2, 3) of its head's row
+  uint32_t qa[KK][2];
+  {
+    const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.Hq + (head_ok ? h0 + gq : h0)) * D +
+                                                       QE * c);
+#pragma unroll
+    for (int i = 0; i < QE / 8; ++i) {
+      const uint4 v = qrow[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t x = head_ok ? w[e] : 0u;
+        if constexpr (EB == 1) x = pack_f16x2(bf16lo_to_f32(x), bf16hi_to_f32(x));
+        qa[(4 * i + e) >> 1][e & 1] = x;
+      }
+    }
+  }
+  const float cmul = p.c * (p.k_scale != nullptr ? p.k_scale[static_cast<size_t>(b) * p.Hkv + kvh] : 1.f);
+  float m = -INFINITY, l = 0.f;
+  float o[NJ][2];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) o[j][0] = o[j][1] = 0.f;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % Cfg::kStages;
+    if (!mbar_wait(&full_bar[s], static_cast<uint32_t>(t / Cfg::kStages) & 1u, abort_p, kDecodeWaitTimeoutNs))
+      break;
+    const uint8_t* kt = sK + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
+    const uint8_t* vt = sV + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
+    const int key0 = start + t * Cfg::kTile + warp * 16;  // first key of this warp's block
+    const int nvalid = end - key0;                        // keys of the block inside the split (may be <= 0)
+
+    // ---- S = Q K^T for the block's two groups of 8 keys (key 8 nt + gq of the block is this
+    //      thread's column)
+    float sc[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint4* krow = reinterpret_cast<const uint4*>(kt + (8 * nt + gq) * Cfg::kRowBytes + QE * EB * c);
+      float acc[2] = {0.f, 0.f};
+      // one 16-byte piece at a time: 2 MMAs of bf16, 4 of E4M3 codes
+#pragma unroll
+      for (int i = 0; i < KW / 4; ++i) {
+        const uint4 v = krow[i];
+        const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (EB == 2) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) mma_16816<EB>(acc, qa[2 * i + h][0], qa[2 * i + h][1], kw[2 * h], kw[2 * h + 1]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            mma_16816<EB>(acc, qa[4 * i + h][0], qa[4 * i + h][1], e4m3x2_to_f16x2(kw[h]), e4m3x2_to_f16x2(kw[h] >> 16));
+        }
+      }
+      // keys 8 nt + 2c and 8 nt + 2c + 1 of the block, base-2 scaled; keys past the split end: -inf
+      sc[nt][0] = (8 * nt + 2 * c < nvalid) ? acc[0] * cmul : -INFINITY;
+      sc[nt][1] = (8 * nt + 2 * c + 1 < nvalid) ? acc[1] * cmul : -INFINITY;
+    }
+
+    // ---- online softmax per head (row gq; the 4 threads of a group share it). The base only
+    //      moves when a score exceeds it by more than 2^8; then the block maximum is formed.
+    const float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    float corr = 1.f;
+    if (__any_sync(0xFFFFFFFFu, mx > m + kDecodeRescaleThreshold)) {
+      float mt = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 2));
+      const float m_cand = fmaxf(m, mt);
+      if (m_cand > m + kDecodeRescaleThreshold) {
+        corr = ex2_approx(m - m_cand);  // 0 when m was -inf
+        m = m_cand;
+      }
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        o[j][0] *= corr;
+        o[j][1] *= corr;
+      }
+    }
+    const float base = (m == -INFINITY) ? 0.f : m;
+    float pw[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      pw[nt][0] = ex2_approx(sc[nt][0] - base);
+      pw[nt][1] = ex2_approx(sc[nt][1] - base);
+    }
+    l = l * corr + ((pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]));
+    const uint32_t pa0 = (EB == 2) ? pack_bf16x2(pw[0][0], pw[0][1]) : pack_f16x2(pw[0][0], pw[0][1]);
+    const uint32_t pa2 = (EB == 2) ? pack_bf16x2(pw[1][0], pw[1][1]) : pack_f16x2(pw[1][0], pw[1][1]);
+
+    // ---- O += P V: B of MMA j holds V rows (2c, 2c+1) and (2c+8, 2c+9) of the block at output
+    //      column VE gq + j. Rows past the split end are zeroed (their shared memory may hold
+    //      anything, and 0 * NaN would not be 0).
+    // in halves of the output columns (16-byte pieces of the four rows), to keep registers low
+    constexpr int kHalves = (VW >= 8) ? 2 : 1;
+    constexpr int HW = VW / kHalves;  // 32-bit words of a row per half
+    constexpr int HJ = NJ / kHalves;  // MMAs per half
+#pragma unroll
+    for (int hf = 0; hf < kHalves; ++hf) {
+      uint32_t vw[4][HW];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = 2 * c + (r & 1) + 8 * (r >> 1);
+        const bool ok = row < nvalid;
+        const uint8_t* vrow = vt + row * Cfg::kRowBytes + VE * EB * gq + hf * HW * 4;
+        if constexpr (HW >= 4) {
+#pragma unroll
+          for (int i = 0; i < HW / 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(vrow + i * 16);
+            vw[r][4 * i] = ok ? v.x : 0u;
+            vw[r][4 * i + 1] = ok ? v.y : 0u;
+            vw[r][4 * i + 2] = ok ? v.z : 0u;
+            vw[r][4 * i + 3] = ok ? v.w : 0u;
+          }
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(vrow);
+          vw[r][0] = ok ? v.x : 0u;
+          vw[r][1] = ok ? v.y : 0u;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < HJ; ++jj) {
+        const int j = hf * HJ + jj;
+        uint32_t b0, b1;
+        if constexpr (EB == 2) {
+          // element j of rows (2c, 2c+1) into one register, likewise rows (2c+8, 2c+9)
+          const uint32_t sel = (jj & 1) ? 0x7632u : 0x5410u;
+          b0 = __byte_perm(vw[0][jj >> 1], vw[1][jj >> 1], sel);
+          b1 = __byte_perm(vw[2][jj >> 1], vw[3][jj >> 1], sel);
+        } else {
+          // codes j of rows (2c, 2c+1) -> one f16 pair, likewise rows (2c+8, 2c+9)
+          const uint32_t sel = (jj & 2) ? 0x7362u : 0x5140u;
+          const uint32_t w01 = __byte_perm(vw[0][jj >> 2], vw[1][jj >> 2], sel);
+          const uint32_t w23 = __byte_perm(vw[2][jj >> 2], vw[3][jj >> 2], sel);
+          b0 = e4m3x2_to_f16x2((jj & 1) ? (w01 >> 16) : w01);
+          b1 = e4m3x2_to_f16x2((jj & 1) ? (w23 >> 16) : w23);
+        }
+        mma_16816<EB>(o[j], pa0, pa2, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[s]);
+  }
+  __syncwarp();
+
+  // l: the 4 threads of a group hold disjoint keys' sums
+  l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+  l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+
+  // merge the consumer warps through shared memory (the stages are free now). This thread holds
+  // O[head gq][VE (2c + e) + j] in o[j][e].
+  named_bar_sync(1, 32 * Cfg::kConsumerWarps);
+  float* red = reinterpret_cast<float*>(smem);  // [warps][8 heads][D + 2]
+  constexpr int kRow = D + 2;
+  {
+    float* r = red + (warp * 8 + gq) * kRow;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      r[VE * (2 * c) + j] = o[j][0];
+      r[VE * (2 * c + 1) + j] = o[j][1];
+    }
+    if (c == 0) {
+      r[D] = m;
+      r[D + 1] = l;
+    }
+  }
+  named_bar_sync(1, 32 * Cfg::kConsumerWarps);
+  const float vmul = p.v_scale != nullptr ? p.v_scale[static_cast<size_t>(b) * p.Hkv + kvh] : 1.f;
+  for (int idx = threadIdx.x; idx < nh * D; idx += 32 * Cfg::kConsumerWarps) {
+    const int gh = idx / D;
+    const int e = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < Cfg::kConsumerWarps; ++w) M = fmaxf(M, red[(w * 8 + gh) * kRow + D]);
+    const float base = (M == -INFINITY) ? 0.f : M;
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < Cfg::kConsumerWarps; ++w) {
+      const float* r = red + (w * 8 + gh) * kRow;
+      const float wt = ex2_approx(r[D] - base);
+      acc += wt * r[e];
+      lsum += wt * r[D + 1];
+    }
+    const size_t slot = (static_cast<size_t>(b) * p.Hq + h0 + gh) * p.S + split;
+    p.o_part[slot * D + e] = acc * vmul;
+    if (e == 0) {
+      p.ml_part[slot * 2] = M;
+      p.ml_part[slot * 2 + 1] = lsum;
+    }
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
 // One CTA of D/64 warps per (sequence, query head); warp w owns output elements [64 w, 64 w + 64),
 // two per lane. The partials of up to 32 splits are loaded in one go, together with the sequence
 // length: a split past the length was never written and is dropped by predicate (its bytes are
@@ -516,6 +849,25 @@ static cudaError_t launch_split_g(const DecodeParams& p, int B, cudaStream_t str
   }
 }
 
+template <int D, int EB>
+static cudaError_t launch_split_mma(const DecodeParams& p, int B, cudaStream_t stream) {
+  using Cfg = DecodeCfg<D, EB, kMmaStages>;
+  auto kern = decode_split_mma_kernel<D, EB>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const dim3 grid(p.S, p.Hkv * p.n_hblk, B);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// The split kernel's consumers: tensor-core MMAs (decode_split_mma_kernel), unless the
+// environment variable GB300_ATTN_DECODE is "ffma" (decode_split_kernel; the same result up to
+// rounding).
+static bool use_mma_split() {
+  const char* e = std::getenv("GB300_ATTN_DECODE");
+  return !(e != nullptr && std::strcmp(e, "ffma") == 0);
+}
+
 // Returns the number of kernels launched through *launched. k_scale/v_scale non-null
 // selects the E4M3 cache (one byte per element), else the cache is bf16.
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const float* k_scale, const float* v_scale,
@@ -542,8 +894,13 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const f
   p.C = C;
   p.c = scale * 1.4426950408889634f;
   if (static_cast<long long>(Hkv) * p.n_hblk > 65535) return cudaErrorInvalidValue;
-  cudaError_t err = fp8 ? ((d == 64) ? launch_split_g<64, 1>(p, B, stream) : launch_split_g<128, 1>(p, B, stream))
-                        : ((d == 64) ? launch_split_g<64, 2>(p, B, stream) : launch_split_g<128, 2>(p, B, stream));
+  cudaError_t err;
+  if (use_mma_split())
+    err = fp8 ? ((d == 64) ? launch_split_mma<64, 1>(p, B, stream) : launch_split_mma<128, 1>(p, B, stream))
+              : ((d == 64) ? launch_split_mma<64, 2>(p, B, stream) : launch_split_mma<128, 2>(p, B, stream));
+  else
+    err = fp8 ? ((d == 64) ? launch_split_g<64, 1>(p, B, stream) : launch_split_g<128, 1>(p, B, stream))
+              : ((d == 64) ? launch_split_g<64, 2>(p, B, stream) : launch_split_g<128, 2>(p, B, stream));
   if (err != cudaSuccess) return err;
   *launched = 1;
   // The combine is launched with programmatic stream serialisation: its grid can be set up
