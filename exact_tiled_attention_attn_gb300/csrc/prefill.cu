@@ -425,27 +425,32 @@ __global__ void __launch_bounds__(352, 1)
       if (ok) {
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld128(t_s, sr);
       const int j0 = j * 128;
+      // blocks past the diagonal or the end of the keys need the element mask before the
+      // maximum; every other block takes the row maximum from the reducing TMEM load
       const bool need_mask = (j0 + 128 > p.Tk) || (p.causal && j0 + 127 > row0);
-      if (need_mask) {
+      float m_raw;
+      if (!need_mask) {
+        m_raw = tmem_ld128_max(t_s, sr);
+      } else {
+        tmem_ld128(t_s, sr);
         const int lim = p.causal ? min(p.Tk - 1, row) : (p.Tk - 1);  // last visible key of this row
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (j0 + k > lim) sr[k] = __float_as_uint(-INFINITY);
+        // row max over columns 0..127: 8 independent chains of 3-input max, merged at the end
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+#pragma unroll
+        for (int k = 16; k < 128; k += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mx[i] = fmax3(mx[i], __uint_as_float(sr[k + 2 * i]), __uint_as_float(sr[k + 2 * i + 1]));
+        }
+        m_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       }
-      // row max over columns 0..127: 8 independent chains (pairwise seeds, then 7 rounds of
-      // 3-input max), merged at the end
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
-#pragma unroll
-      for (int k = 16; k < 128; k += 16) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          mx[i] = fmax3(mx[i], __uint_as_float(sr[k + 2 * i]), __uint_as_float(sr[k + 2 * i + 1]));
-      }
-      const float m_blk = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+      const float m_blk = m_raw * c;
       const float m_cand = fmaxf(m_run, m_blk);
       const bool grow = m_cand > m_run + kRescaleThreshold;
       float corr = 1.f;
