@@ -43,19 +43,27 @@ NORM = W.NORM_QWEN
 WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch on the prefill workload, from the
-# ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md,
-# with the SHA-256 of the kernel source it was taken with: the figure is reported only while
-# that source is unchanged.
-PREFILL_TRAFFIC = {"bytes": 348698368 + 94247424,
-                   "prefill_cu_sha256": "ac5507e5c8398274bc66cf7a2f464edd09c3375f54872300994bf8ce3d427e21"}
+# ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md, with
+# the SHA-256 of the kernel's sources (prefill.cu and common.cuh) it was taken with: the figure is
+# reported only while those sources are unchanged.
+PREFILL_TRAFFIC = {"bytes": 353455616 + 95549696,
+                   "sources_sha256": "6c78e32c29aad2462ca57f4f2c6cfc89aec25e3911933fc71eea61a9a45550ce"}
+PREFILL_SOURCES = ("prefill.cu", "common.cuh")
+
+
+def prefill_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "exact_tiled_attention_attn_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def prefill_traffic():
-    import hashlib
-    path = os.path.join(ROOT, "exact_tiled_attention_attn_gb300", "csrc", "prefill.cu")
-    with open(path, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    return PREFILL_TRAFFIC["bytes"] if sha == PREFILL_TRAFFIC["prefill_cu_sha256"] else None
+    if PREFILL_TRAFFIC["bytes"] is None:
+        return None
+    return PREFILL_TRAFFIC["bytes"] if prefill_sources_sha256() == PREFILL_TRAFFIC["sources_sha256"] else None
 
 
 def _peaks():
@@ -479,7 +487,7 @@ def run_gpu(args):
         dec8 = {"value": round(d8_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                 "frac": round(d8_gbs / peaks["hbm"], 4), "ms": round(d8_ms, 4), "bytes_per_launch": d8_bytes,
                 "vs_bf16_decode_time": round(dec_ms / d8_ms, 3),
-                "kernels": "decode_split_kernel<128,4,1> (E4M3 cache) + decode_combine_kernel<128>",
+                "kernels": "decode_split_mma_kernel<128,1> (E4M3 cache) + decode_combine_kernel<128>",
                 "num_splits": splits}
         del kq, vq
 
@@ -598,7 +606,7 @@ def run_gpu(args):
                          "flops_per_launch": flops},
             "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                        "frac": round(dec_gbs / peaks["hbm"], 4), "bytes_per_launch": dec_bytes,
-                       "kernels": "decode_split_kernel<128,4> + decode_combine_kernel<128>",
+                       "kernels": "decode_split_mma_kernel<128,2> + decode_combine_kernel<128>",
                        "num_splits": splits},
             "rmsnorm": {"value": norm_graph["GB/s"], "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                         "frac": norm_graph["frac"], "bytes_per_launch": norm_bytes,
