@@ -103,15 +103,17 @@ size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
 
 int attn_decode_default_splits(int B, int Hkv, int Lcap) {
   if (B < 1 || Hkv < 1 || Lcap < 1) return 1;
-  // Chunks of about 1024 keys (the split kernel streams a chunk through a 4-stage ring;
-  // measured best at 32-40 splits for 16 sequences of up to 32768 keys); at least enough
-  // splits for ~4 thread blocks per SM of a 152-SM part when the batch is small.
+  // Chunks of about 1024 keys (measured best at 32 splits for 16 sequences of up to 32768 keys);
+  // at least enough splits for ~2 thread blocks per SM of a 152-SM part when the batch is small
+  // (the split kernel runs 2 per SM; measured, B16 Hkv8 d128, Lcap 2048: 2 splits 7 % faster
+  // than 4).
   int s = (Lcap + 1023) / 1024;
-  const long long want = (4LL * 152 + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
+  const long long want = (2LL * 152 + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
   if (s < want) s = want > (1 << 20) ? (1 << 20) : static_cast<int>(want);
   // Rounded down to a power of two: with a power-of-two cache length every chunk is then a whole
-  // number of the kernel's 64-row stages (measured, B16 Hkv8 d128: Lcap 2048, 4 splits 23.7 us per
-  // step vs 28.3 us with 5; Lcap 8192, 8 splits 75.3 vs 90.6 with 6; Lcap 32768, 32 splits best).
+  // number of the kernel's 64-row stages (measured with the earlier FFMA split kernel, B16 Hkv8
+  // d128: Lcap 2048, 4 splits 23.7 us per step vs 28.3 us with 5; Lcap 8192, 8 splits 75.3 vs
+  // 90.6 with 6).
   int p2 = 1;
   while (p2 <= s / 2) p2 *= 2;
   s = p2;

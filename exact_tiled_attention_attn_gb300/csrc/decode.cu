@@ -482,15 +482,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Three stages per CTA and two CTAs per SM (the same bytes in flight per SM as the FFMA kernel's
-// two stages and three CTAs; at d = 128 this kernel needs ~168 registers per thread).
-constexpr int kMmaStages = 3;
+// Two CTAs per SM (at d = 128 this kernel needs ~168 registers per thread) and 3 stages of 64
+// rows, 6 for the 1-byte rows of an E4M3 cache at d = 128 (96 KB of K and V per CTA, as with
+// bf16 rows). Measured on the B16 Hq32 Hkv8 L ~ U[8192, 32768] decode: E4M3 d = 128, 6 stages
+// 5205 GB/s against 5090 with 3; E4M3 d = 64, 12 stages 4008 against 4481 with 3; bf16 d = 64,
+// 6 stages no faster than 3.
 constexpr int kMmaCtasPerSm = 2;
+template <int D, int EB>
+__host__ __device__ constexpr int mma_stages() {
+  return (EB == 1 && D == 128) ? 6 : 3;
+}
 
 template <int D, int EB>
-__global__ void __launch_bounds__(DecodeCfg<D, EB, kMmaStages>::kThreads, kMmaCtasPerSm)
+__global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThreads, kMmaCtasPerSm)
     decode_split_mma_kernel(const DecodeParams p) {
-  using Cfg = DecodeCfg<D, EB, kMmaStages>;
+  using Cfg = DecodeCfg<D, EB, mma_stages<D, EB>()>;
   static_assert(Cfg::kTile == 16 * Cfg::kConsumerWarps, "one 16-key block per consumer warp per stage");
   constexpr int KK = D / 16;          // MMAs along d for S
   constexpr int NJ = D / 8;           // MMAs along the output columns for O
@@ -851,7 +857,7 @@ static cudaError_t launch_split_g(const DecodeParams& p, int B, cudaStream_t str
 
 template <int D, int EB>
 static cudaError_t launch_split_mma(const DecodeParams& p, int B, cudaStream_t stream) {
-  using Cfg = DecodeCfg<D, EB, kMmaStages>;
+  using Cfg = DecodeCfg<D, EB, mma_stages<D, EB>()>;
   auto kern = decode_split_mma_kernel<D, EB>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
