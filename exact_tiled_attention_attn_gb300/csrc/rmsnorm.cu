@@ -106,6 +106,12 @@ __device__ __forceinline__ void store_segment(const uint4 (&v)[VPL], const uint4
   }
 }
 
+// Start pulling `bytes` at `src` into L2 (an asynchronous bulk prefetch: no data returns to the
+// SM, nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float combine8(const float (&s)[8]) {
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
@@ -116,15 +122,21 @@ template <int NSEG, int VPL, bool RES>
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const uint4* __restrict__ x, const uint4* __restrict__ res,
                                                            const uint4* __restrict__ w, uint4* __restrict__ y,
                                                            uint4* __restrict__ h, int T, int D, float eps) {
-  // launched with programmatic stream serialisation (see launch_shape): wait until the previous
-  // kernel on the stream has completed and its writes are visible, then let the next launch be set up
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  // Launched with programmatic stream serialisation (see launch_shape). The row is first
+  // prefetched into L2, which may overlap the previous kernel's end: L2 is where the previous
+  // kernel's writes land, so this cannot make the loads below see old data. Then wait until the
+  // previous kernel has completed and its writes are visible, and let the next launch be set up.
   constexpr int kRounds = NSEG == 8 ? 4 : 1;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= T) return;
   const int nvec = D >> 3;
+  if (lane == 0 && row < T) {
+    prefetch_l2(x + static_cast<size_t>(row) * nvec, static_cast<uint32_t>(D) * 2);
+    if (RES) prefetch_l2(res + static_cast<size_t>(row) * nvec, static_cast<uint32_t>(D) * 2);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (row >= T) return;
   const int seg_vecs = nvec / NSEG;
   const int half = lane >> 4, vl = lane & 15;
   const size_t off = static_cast<size_t>(row) * nvec;
@@ -166,14 +178,18 @@ template <int NSEG, int VPL, bool RES>
 __global__ void __launch_bounds__(32 * kNormSplitWarps) rmsnorm_split_kernel(
     const uint4* __restrict__ x, const uint4* __restrict__ res, const uint4* __restrict__ w, uint4* __restrict__ y,
     uint4* __restrict__ h, int D, float eps) {
-  // launched with programmatic stream serialisation (see launch_shape): wait until the previous
-  // kernel on the stream has completed and its writes are visible, then let the next launch be set up
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
+  // launched with programmatic stream serialisation: the row is prefetched into L2 first, as in
+  // rmsnorm_warp_kernel, then the kernel waits for the previous one
   __shared__ float seg_sum[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row = blockIdx.x;
   const int nvec = D >> 3;
+  if (threadIdx.x == 0) {
+    prefetch_l2(x + static_cast<size_t>(row) * nvec, static_cast<uint32_t>(D) * 2);
+    if (RES) prefetch_l2(res + static_cast<size_t>(row) * nvec, static_cast<uint32_t>(D) * 2);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int seg_vecs = nvec / NSEG;
   const int half = lane >> 4, vl = lane & 15;
   const int seg = 2 * warp + half;
