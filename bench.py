@@ -78,6 +78,88 @@ def _peaks():
 
 # ----------------------------------------------------------------------------- clocks
 
+def summarise_clock_samples(samples, t0: float, t1: float, source: str):
+    """Median SM clock, highest max clock and the union of the named clock-event reasons over
+    the samples (wall time, sm MHz, max MHz, set of reason names) taken between t0 and t1."""
+    sm, smax, reasons = [], [], set()
+    for ts, mhz, max_mhz, names in samples:
+        if t0 <= ts <= t1:
+            sm.append(float(mhz))
+            smax.append(float(max_mhz))
+            reasons.update(names)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+            "reasons": sorted(reasons), "source": source}
+
+
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) and the names reported for them.
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+
+def nvml_reason_names(mask: int):
+    return {name for bit, name in NVML_REASONS.items() if mask & bit}
+
+
+class NvmlClockSampler:
+    """Polls the SM clock and the clock-event reasons through NVML every `period_s` in a thread.
+
+    Read-only queries (nvmlDeviceGetClockInfo, nvmlDeviceGetMaxClockInfo,
+    nvmlDeviceGetCurrentClocksEventReasons); a timed region of a few tens of milliseconds still
+    holds several samples, which the 200 ms nvidia-smi loop cannot give. `lib` is the loaded
+    libnvidia-ml (a stand-in object in the CPU tests). Raises OSError when NVML is unusable.
+    """
+
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str, lib=None, period_s: float = 0.002):
+        import ctypes
+        self.ct = ctypes
+        self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+            self.lib.nvmlShutdown()
+            raise OSError("no NVML device with uuid " + uuid)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if self.reasons_fn is None:
+            self.reasons_fn = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _sample(self):
+        ct = self.ct
+        mhz, max_mhz, mask = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, self.CLOCK_SM, ct.byref(mhz)) != 0:
+            return None
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.CLOCK_SM, ct.byref(max_mhz)) != 0:
+            return None
+        if self.reasons_fn(self.handle, ct.byref(mask)) != 0:
+            return None
+        return (time.time(), mhz.value, max_mhz.value, nvml_reason_names(mask.value))
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            s = self._sample()
+            if s is not None:
+                self.samples.append(s)
+            self.stop_flag.wait(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self, t0: float, t1: float):
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        self.lib.nvmlShutdown()
+        return summarise_clock_samples(self.samples, t0, t1, f"nvml every {self.period * 1e3:g} ms")
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons every 200 ms in a subprocess."""
 
@@ -106,6 +188,22 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
+    @staticmethod
+    def parse(lines):
+        """(wall time, csv line) pairs -> samples as summarise_clock_samples takes them."""
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        out = []
+        for ts, ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                mhz, max_mhz = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            out.append((ts, mhz, max_mhz, {n for n, v in zip(names, parts[4:8]) if v.lower() == "active"}))
+        return out
+
     def stop(self, t0: float, t1: float):
         """Stop sampling; summarise the samples that arrived between t0 and t1 (wall time)."""
         if self.proc is None:
@@ -117,26 +215,17 @@ class ClockSampler:
             self.proc.kill()
         if self.thread is not None:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, ln in self.lines:
-            if ts < t0 or ts > t1:
-                continue
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return summarise_clock_samples(self.parse(self.lines), t0, t1, "nvidia-smi every 200 ms")
+
+
+def make_clock_sampler(uuid, local_index):
+    """NVML polling when the library answers for this device, else the nvidia-smi loop."""
+    if uuid:
+        try:
+            return NvmlClockSampler(uuid)
+        except (OSError, AttributeError):
+            pass
+    return ClockSampler(uuid if uuid else local_index)
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -230,7 +319,7 @@ def run_gpu(args):
         uuid = u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         uuid = None
-    sampler = ClockSampler(uuid if uuid else local)
+    sampler = make_clock_sampler(uuid, local)
     sampler.start()
     time.sleep(0.4)
     if world > 1:
