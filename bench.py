@@ -450,14 +450,18 @@ def run_gpu(args):
             pq, pk, pv = [t.to(dev) for t in W.attention_inputs(shp)]
             po = torch.empty_like(pq)
             pl = torch.empty(shp.B, shp.Hq, shp.T, dtype=torch.float32, device=dev)
+            pws = torch.empty(attn.fwd_workspace_size(shp.d), dtype=torch.uint8, device=dev)
             for _ in range(3):
-                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl)
+                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl, workspace=pws)
+            n_launch0 = attn.kernel_launches()
+            attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl, workspace=pws)
+            launches_per_call = attn.kernel_launches() - n_launch0
             tms = []
             for _ in range(20):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl)
+                attn.fwd(pq, pk, pv, causal=shp.causal, scale=shp.scale, out=po, lse=pl, workspace=pws)
                 b.record(stream)
                 torch.cuda.synchronize()
                 tms.append(a.elapsed_time(b))
@@ -469,9 +473,12 @@ def run_gpu(args):
                                   "peak": peaks["bf16"], "frac": round(p_tf / peaks["bf16"], 4),
                                   "ms": round(p_ms, 4), "ms_p10_p90": [round(tms[2], 4), round(tms[-3], 4)],
                                   "flops_per_launch": shp.flops(), "workload": shp.name,
-                                  "kernel": f"attn_fwd_kernel<{shp.d}>",
-                                  "timing": "median of 20 launches, each between two events, L2 flushed before it"}
-            del pq, pk, pv, po, pl
+                                  "kernel": f"attn_fwd_kernel<{shp.d}>" + (
+                                      f" + attn_fwd_merge_kernel<{shp.d}> (last round's units split along the keys)"
+                                      if launches_per_call == 2 else ""),
+                                  "launches_per_call": launches_per_call,
+                                  "timing": "median of 20 calls, each between two events, L2 flushed before it"}
+            del pq, pk, pv, po, pl, pws
         del flush
 
     # ---- RMSNorm at growing T: the workload's 16.8 MB is launch- and latency-bound,

@@ -21,7 +21,7 @@ import torch
 from . import _lib
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["fwd", "bwd", "decode", "decode_noalloc", "noalloc_splits", "NOALLOC_SCRATCH_BYTES", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
+__all__ = ["fwd", "fwd_workspace_size", "bwd", "decode", "decode_noalloc", "noalloc_splits", "NOALLOC_SCRATCH_BYTES", "decode_fp8", "kv_quantize_fp8", "rmsnorm", "rmsnorm_residual",
            "decode_workspace_size",
            "default_splits",
            "last_device_error", "kernel_launches", "selftest_wait_timeout", "AttnError", "lib"]
@@ -50,11 +50,18 @@ def _check_tensor(name, t, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
+def fwd_workspace_size(d: int) -> int:
+    return int(_lib.load().attn_fwd_workspace_size(d))
+
+
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-        return_lse: bool = True, stream=None):
+        return_lse: bool = True, stream=None, workspace=None):
     """Exact attention O = softmax(scale * Q K^T + mask) V (bf16 in/out), and the fp32 LSE.
 
     q [B, Hq, Tq, d], k/v [B, Hkv, Tk, d], contiguous bf16 on one CUDA device.
+    A non-causal call takes a scratch ``workspace`` (uint8 tensor of at least
+    ``fwd_workspace_size(d)`` bytes; allocated when not given) that lets the library
+    balance its last round of work; causal calls need none.
     """
     _check_tensor("q", q, torch.bfloat16, 4)
     _check_tensor("k", k, torch.bfloat16, 4)
@@ -71,10 +78,17 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         _check_tensor("out", out, torch.bfloat16, 4)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
-    st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              lse.data_ptr() if lse is not None else None,
-                              B, Hq, Hkv, Tq, Tk, d, 1 if causal else 0, float(scale), _stream_ptr(stream))
-    _lib.check("attn_fwd", st)
+    if workspace is None and not causal and d in (64, 128):
+        workspace = torch.empty(fwd_workspace_size(d), dtype=torch.uint8, device=q.device)
+        if stream is not None:
+            workspace.record_stream(stream)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.load().attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None,
+                                 B, Hq, Hkv, Tq, Tk, d, 1 if causal else 0, float(scale), ws_ptr, ws_bytes,
+                                 _stream_ptr(stream))
+    _lib.check("attn_fwd_ws", st)
     return out, lse
 
 

@@ -26,6 +26,8 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_workspace_size": (ctypes.c_size_t, [_I]),
+    "attn_fwd_ws": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.c_size_t, _P]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, ctypes.c_size_t, _P]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),

@@ -9,7 +9,9 @@
 
 namespace gb300 {
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                            int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream);
+                            int Tq, int Tk, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream, int* launched);
+size_t prefill_workspace_bytes(int d);
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const float* k_scale, const float* v_scale,
                           const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap,
                           float scale, int S, int C, void* workspace, cudaStream_t stream, int* launched);
@@ -78,8 +80,19 @@ using namespace gb300;
 
 extern "C" {
 
+size_t attn_fwd_workspace_size(int d) {
+  if (d != 64 && d != 128) return 0;
+  return prefill_workspace_bytes(d);
+}
+
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+  return attn_fwd_ws(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, nullptr, 0, stream);
+}
+
+attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Tq, int Tk, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -90,9 +103,16 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
   if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
     return ATTN_ERR_INVALID_ARG;
-  const cudaError_t err = launch_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
+  if (workspace == nullptr && workspace_bytes != 0) return ATTN_ERR_WORKSPACE;
+  if (workspace != nullptr) {
+    if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    if (workspace_bytes < attn_fwd_workspace_size(d)) return ATTN_ERR_WORKSPACE;
+  }
+  int launched = 0;
+  const cudaError_t err = launch_attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, workspace,
+                                          workspace_bytes, stream, &launched);
+  g_launches.fetch_add(static_cast<unsigned long long>(launched));
   if (err != cudaSuccess) return ATTN_ERR_CUDA;
-  g_launches.fetch_add(1);
   return ATTN_OK;
 }
 

@@ -38,6 +38,7 @@
 // which finite base is subtracted ("Module 07", section "Online softmax: derivation":
 // the factor exp(m - c) cancels between numerator and denominator), and the bound
 // keeps every p <= 256, far inside fp32 and bf16 range.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 
@@ -83,7 +84,13 @@ struct PrefillParams {
   int pair_heads;  // 1: tiles are heads (2p, 2p+1) at the same rows; 0: row tiles (2p, 2p+1) of one head
   int n_qt;        // number of query tiles of 128 rows
   int units;       // work units (pairs of query tiles), heaviest first when causal
-  float c;         // scale * log2(e)
+  // Key-split tail (see decode_item): units [0, full_units) run whole; each later unit runs as
+  // `split` pieces over consecutive ranges of its key blocks, whose partial results go to
+  // part_o / part_lse2 and are merged by attn_fwd_merge_kernel. items = the work items.
+  int full_units, split, items;
+  float* part_o;     // [piece][tile 2][row 128][D] fp32, O of the piece normalised by its own l
+  float* part_lse2;  // [piece][tile 2][row 128] fp32, m + log2 l of the piece (base 2, scaled scores)
+  float c;           // scale * log2(e)
 };
 
 struct UnitInfo {
@@ -91,6 +98,8 @@ struct UnitInfo {
   int head[2];
   int row0[2];
   int nkv[2];  // key tiles to visit per query tile (0 = tile inactive)
+  int kb0;     // first key block (0 unless the item is a piece of a split unit)
+  int part;    // piece index into part_o / part_lse2, or -1 for a whole unit
 };
 
 __device__ __forceinline__ int kv_tiles_for(const PrefillParams& p, int row0) {
@@ -132,6 +141,34 @@ __device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit
   return u;
 }
 
+// Work item -> unit or piece of a unit. A piece covers key blocks [kb0, kb1) of its unit, a
+// share of the unit's n blocks; only units whose two tiles visit the same blocks (non-causal)
+// are split, so both tiles of a piece visit all of its blocks (or tile 1 none, past Tq).
+// kSplit = false: the launch has no split units, so every item is a whole unit.
+template <bool kSplit>
+__device__ __forceinline__ UnitInfo decode_item(const PrefillParams& p, int item) {
+  if (!kSplit) {
+    UnitInfo u = decode_unit(p, item);
+    u.kb0 = 0;
+    u.part = -1;
+    return u;
+  }
+  // one straight-line path for whole units (one piece of all n blocks) and pieces (measured:
+  // the branchy form made the compiler spill registers in the softmax warps)
+  const bool whole = item < p.full_units;
+  const int t = item - p.full_units;
+  const int s = whole ? 1 : p.split;
+  const int pc = whole ? 0 : t % p.split;
+  UnitInfo u = decode_unit(p, whole ? item : p.full_units + t / p.split);
+  const int n = max(u.nkv[0], u.nkv[1]);
+  const int kb0 = pc * n / s, kb1 = (pc + 1) * n / s;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) u.nkv[q] = max(0, min(u.nkv[q], kb1) - kb0);
+  u.kb0 = kb0;
+  u.part = whole ? -1 : t;
+  return u;
+}
+
 // Key block j has MMA work iff some tile issues S_q(j) (j < nkv_q) or PV_q(j-1) (0 < j <= nkv_q).
 __device__ __forceinline__ bool block_has_work(const UnitInfo& u, int j) {
   const int n = max(u.nkv[0], u.nkv[1]);
@@ -147,7 +184,7 @@ __device__ __forceinline__ int unit_index(int round) {
                      : base + static_cast<int>(blockIdx.x);
 }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(352, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -204,6 +241,9 @@ __global__ void __launch_bounds__(352, 1)
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
+      // Q is read once per unit: evict it first, so that L2 keeps the K/V blocks the other
+      // CTAs of the head group still read.
+      const uint64_t q_policy = l2_policy_evict_first();
       int G = 0, U = 0;
       int slot = 0;        // slot of the next item
       int filled = 0;      // items loaded so far (saturates at kSlots)
@@ -222,10 +262,10 @@ __global__ void __launch_bounds__(352, 1)
         return true;
       };
       bool alive = true;
-      for (int round = 0; alive && round * static_cast<int>(gridDim.x) < p.units; ++round) {
+      for (int round = 0; alive && round * static_cast<int>(gridDim.x) < p.items; ++round) {
         const int idx = unit_index(round);
-        if (idx >= p.units) continue;
-        const UnitInfo u = decode_unit(p, idx);
+        if (idx >= p.items) continue;
+        const UnitInfo u = decode_item<kSplit>(p, idx);
         const int n_iter = max(u.nkv[0], u.nkv[1]);
         // this unit's Q overwrites the previous one's: wait for its last S MMAs (block G - 2)
         if (U > 0 && !wait_block(G - 2)) break;
@@ -234,8 +274,8 @@ __global__ void __launch_bounds__(352, 1)
         for (int q = 0; q < 2; ++q) {
           if (u.nkv[q] == 0) continue;
           for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-            tma_load_3d(sQ + q * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmQ, &q_full, kb * 64, u.row0[q],
-                        u.b * p.Hq + u.head[q]);
+            tma_load_3d_hint(sQ + q * Cfg::kTileBytes + kb * Cfg::kBoxBytes, &tmQ, &q_full, kb * 64, u.row0[q],
+                             u.b * p.Hq + u.head[q], q_policy);
         }
         const int zkv = u.b * p.Hkv + u.kvh;
         const int n_items = 2 * n_iter;  // item 2j = K(j), item 2j + 1 = V(j)
@@ -258,7 +298,8 @@ __global__ void __launch_bounds__(352, 1)
           }
           const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
           for (int kb = 0; kb < Cfg::kNumBox; ++kb)
-            tma_load_3d(sKV + slot * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, rb, kb * 64, (i >> 1) * 128, zkv);
+            tma_load_3d(sKV + slot * Cfg::kTileBytes + kb * Cfg::kBoxBytes, map, rb, kb * 64,
+                        (u.kb0 + (i >> 1)) * 128, zkv);
           if (++slot == Cfg::kSlots) slot = 0;
         }
         G += n_iter + 1;
@@ -288,10 +329,10 @@ __global__ void __launch_bounds__(352, 1)
       // them to the issuer (kBarData) and waits for the issuer's acknowledgement
       // (kBarDataAck) before looking at block j + 1, so the two warps stay in lockstep.
       int G = 0, U = 0;
-      for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.items; ++round) {
         const int idx = unit_index(round);
-        if (idx >= p.units) continue;
-        const UnitInfo u = decode_unit(p, idx);
+        if (idx >= p.items) continue;
+        const UnitInfo u = decode_item<kSplit>(p, idx);
         const int n_iter = max(u.nkv[0], u.nkv[1]);
         if (lane == 0) mbar_wait(&q_full, static_cast<uint32_t>(U) & 1u, abort_p, kPrefillWaitTimeoutNs);
         for (int j = 0; j <= n_iter; ++j) {
@@ -328,10 +369,10 @@ __global__ void __launch_bounds__(352, 1)
       uint32_t v16 = kRing16 - kTile16;  // slot of V(j-1), used only when j > 0
       bool any_mma = false;
       int G = 0;
-      for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+      for (int round = 0; round * static_cast<int>(gridDim.x) < p.items; ++round) {
         const int idx = unit_index(round);
-        if (idx >= p.units) continue;
-        const UnitInfo u = decode_unit(p, idx);
+        if (idx >= p.items) continue;
+        const UnitInfo u = decode_item<kSplit>(p, idx);
         const int n_iter = max(u.nkv[0], u.nkv[1]);
         const int nkv0 = u.nkv[0], nkv1 = u.nkv[1];
         for (int j = 0; j <= n_iter; ++j) {
@@ -402,10 +443,10 @@ __global__ void __launch_bounds__(352, 1)
     int G = 0;
     int s1_count = 0;  // S_1 blocks committed in earlier units (phases of s_full1)
     int o_count = 0;   // earlier units in which this tile was active (phases of o_done[q])
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.units; ++round) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.items; ++round) {
     const int idx = unit_index(round);
-    if (idx >= p.units) continue;
-    const UnitInfo u = decode_unit(p, idx);
+    if (idx >= p.items) continue;
+    const UnitInfo u = decode_item<kSplit>(p, idx);
     const int n_iter = max(u.nkv[0], u.nkv[1]);
     const int nkv = q ? u.nkv[1] : u.nkv[0];
     const int row0 = q ? u.row0[1] : u.row0[0];
@@ -414,15 +455,19 @@ __global__ void __launch_bounds__(352, 1)
     float m_run = -INFINITY;
     float l_run = 0.f;
 
-    for (int j = 0; j < nkv; ++j) {
+    // j runs over the absolute key blocks jb .. jb + nkv - 1 of the item; the barrier rings
+    // count the item's blocks from G (and s1_count), so they are indexed with j - jb.
+    const int jb = kSplit ? u.kb0 : 0;
+    const int g_j = G - jb, s1_j = s1_count - jb;
+    for (int j = jb; j < jb + nkv; ++j) {
       // S_q(j) ready: tile 1 on s_full1, tile 0 on the per-block barrier that follows S_0(j).
       // After a failed wait the warp skips the work but still arrives on the named barrier
       // below, once per block, so the issuer's syncs always complete.
       if (ok) {
-        const bool w = (q == 1) ? mbar_wait(&s_full1, static_cast<uint32_t>(s1_count + j) & 1u, abort_p,
+        const bool w = (q == 1) ? mbar_wait(&s_full1, static_cast<uint32_t>(s1_j + j) & 1u, abort_p,
                                             kPrefillWaitTimeoutNs)
-                                : mbar_wait(&iter_done[(G + j) % kIterRing],
-                                            static_cast<uint32_t>((G + j) / kIterRing) & 1u, abort_p,
+                                : mbar_wait(&iter_done[(g_j + j) % kIterRing],
+                                            static_cast<uint32_t>((g_j + j) / kIterRing) & 1u, abort_p,
                                             kPrefillWaitTimeoutNs);
         ok = __all_sync(0xFFFFFFFFu, w);
       }
@@ -432,13 +477,15 @@ __global__ void __launch_bounds__(352, 1)
       const int j0 = j * 128;
       // blocks past the diagonal or the end of the keys need the element mask before the
       // maximum; every other block takes the row maximum from the reducing TMEM load
-      const bool need_mask = (j0 + 128 > p.Tk) || (p.causal && j0 + 127 > row0);
+      // (split launches are never causal: kSplit drops the causal terms at compile time)
+      const bool causal = !kSplit && p.causal;
+      const bool need_mask = (j0 + 128 > p.Tk) || (causal && j0 + 127 > row0);
       float m_raw;
       if (!need_mask) {
         m_raw = tmem_ld128_max(t_s, sr);
       } else {
         tmem_ld128(t_s, sr);
-        const int lim = p.causal ? min(p.Tk - 1, row) : (p.Tk - 1);  // last visible key of this row
+        const int lim = causal ? min(p.Tk - 1, row) : (p.Tk - 1);  // last visible key of this row
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (j0 + k > lim) sr[k] = __float_as_uint(-INFINITY);
@@ -484,7 +531,7 @@ __global__ void __launch_bounds__(352, 1)
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       l_run = l_run * corr + ((a01.x + a01.y) + (a23.x + a23.y));
-      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+      if (j > jb && __any_sync(0xFFFFFFFFu, grow)) {
         // O holds the sum up to block j-1 relative to the old base; PV_q(j-1) was issued before
         // S_q(j), so it has completed by now. Rescale in TMEM (after P is written, so the
         // registers of S are free).
@@ -509,7 +556,25 @@ __global__ void __launch_bounds__(352, 1)
       ok = __all_sync(0xFFFFFFFFu,
                       mbar_wait(&o_done[q], static_cast<uint32_t>(o_count) & 1u, abort_p, kPrefillWaitTimeoutNs));
       tc_fence_after();
-      if (ok) {
+      if (kSplit && ok && unit_index(round) >= p.full_units) {
+        // A piece of a split unit: O / l of the piece in fp32 and m + log2 l, for the merge.
+        // (The item index is recomputed from the round rather than kept live across the loop.)
+        const float inv_l = 1.f / l_run;
+        const size_t prow = (static_cast<size_t>(unit_index(round) - p.full_units) * 2 + q) * 128 + row_in_tile;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(t_o + cc * 32, ov);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[cc * 8 + v] = make_float4(__uint_as_float(ov[4 * v]) * inv_l, __uint_as_float(ov[4 * v + 1]) * inv_l,
+                                          __uint_as_float(ov[4 * v + 2]) * inv_l,
+                                          __uint_as_float(ov[4 * v + 3]) * inv_l);
+        }
+        p.part_lse2[prow] = m_run + log2f(l_run);
+      } else if (ok) {
+        const uint64_t o_policy = l2_policy_evict_first();  // O is written once and not read here
         const float inv_l = 1.f / l_run;
         const bool store = row < p.Tq;
         const size_t orow = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row;
@@ -524,7 +589,9 @@ __global__ void __launch_bounds__(352, 1)
           if (store) {
             uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + cc * 32);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              st_global_v4_hint(dst + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]),
+                                o_policy);
           }
         }
         if (store && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
@@ -542,6 +609,79 @@ __global__ void __launch_bounds__(352, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Merge of the pieces of the split units. The pieces of a unit cover disjoint key ranges, so
+// the row's result is their weighted mean with weights l_p 2^(m_p - M) ("Module 07", section
+// "Online softmax: derivation": partial sums over key blocks combine after rescaling to a
+// common base; the same merge as flash-decoding's): O = sum_p w_p O_p / sum_p w_p with
+// w_p = 2^(lse2_p - M), M = max_p lse2_p, and the row's log-sum-exp (M + log2 sum_p w_p) ln 2.
+// One warp per query row of a split unit: lane p reads piece p's log-sum-exp (32 pieces at a
+// time), the maximum and the weights' sum are reduced across the warp (a fixed tree), and the
+// weighted sum of the pieces' rows runs in piece order with lane e holding D/32 consecutive
+// columns, its loads unrolled so that several pieces' rows are in flight at once (the kernel
+// is bound by load latency, not bandwidth). Launched as a programmatic dependent of the
+// prefill kernel.
+template <int D>
+__global__ void __launch_bounds__(256) attn_fwd_merge_kernel(const PrefillParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces' results are complete
+  constexpr int E = D / 32;
+  const int wg = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int t = wg >> 8;  // split unit, 256 rows (2 tiles x 128) each
+  const int q = (wg >> 7) & 1;
+  const int i = wg & 127;
+  if (t >= p.units - p.full_units) return;
+  const UnitInfo u = decode_unit(p, p.full_units + t);
+  const int row = u.row0[q] + i;
+  if (u.nkv[q] == 0 || row >= p.Tq) return;
+  // piece pc of unit t is part t * split + pc: its row i of tile q is at ((part * 2 + q) * 128 + i)
+  const size_t row_p0 = (static_cast<size_t>(t) * p.split * 2 + q) * 128 + i;
+  const float* lse2 = p.part_lse2 + row_p0;
+  float mx = -INFINITY;
+  for (int c = 0; c < p.split; c += 32)
+    if (c + lane < p.split) mx = fmaxf(mx, lse2[static_cast<size_t>(c + lane) * 256]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int c = 0; c < p.split; c += 32) {
+    const int n = min(32, p.split - c);
+    const float w_lane = lane < n ? ex2_approx(lse2[static_cast<size_t>(c + lane) * 256] - mx) : 0.f;
+    float ws = w_lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
+    wsum += ws;
+    const float* src = p.part_o + (row_p0 + static_cast<size_t>(c) * 256) * D + lane * E;
+#pragma unroll 4
+    for (int pc = 0; pc < n; ++pc) {
+      const float w = __shfl_sync(0xFFFFFFFFu, w_lane, pc);
+      const float* r = src + static_cast<size_t>(pc) * 256 * D;
+      if constexpr (E == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(r);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+      } else {
+        const float4 x = *reinterpret_cast<const float4*>(r);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+      }
+    }
+  }
+  const float inv = 1.f / wsum;
+  const size_t orow = (static_cast<size_t>(u.b) * p.Hq + u.head[q]) * p.Tq + row;
+  __nv_bfloat16* dst = p.o + orow * D + lane * E;
+  if constexpr (E == 2) {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  }
+  if (lane == 0 && p.lse != nullptr) p.lse[orow] = (mx + log2f(wsum)) * 0.69314718055994530942f;
 }
 
 // --------------------------------------------------------------------------------------
@@ -564,19 +704,58 @@ static int sm_count() {
   return cached[dev];
 }
 
-// One persistent CTA per SM (the shared memory allows one), or one per unit when there are fewer.
+// Persistent CTAs for the forward kernel: one per SM (the shared memory allows one), or fewer
+// when the environment variable GB300_ATTN_PREFILL_CTAS gives a smaller positive count (a
+// scheduling knob; the tests use it to reach the split tail on small problems).
+static int prefill_ctas() {
+  const int sms = sm_count();
+  const char* e = std::getenv("GB300_ATTN_PREFILL_CTAS");
+  if (e != nullptr) {
+    const int cap = std::atoi(e);
+    if (cap > 0 && cap < sms) return cap;
+  }
+  return sms;
+}
+
+// Scratch for the split tail with `ctas` persistent CTAs: at most ctas pieces of 2 x 128 rows,
+// each row d fp32 values of O and one base-2 log-sum-exp.
+static size_t split_scratch_bytes(int ctas, int d) {
+  return static_cast<size_t>(ctas) * 256 * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+size_t prefill_workspace_bytes(int d) { return split_scratch_bytes(sm_count(), d); }
+
+// The forward kernel on `grid` persistent CTAs, then, when units are split, the merge kernel.
 template <int D>
 static cudaError_t launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                const PrefillParams& p, cudaStream_t stream) {
+                                const PrefillParams& p, int grid, cudaStream_t stream, int* launched) {
   using Cfg = PrefillCfg<D>;
-  auto kern = attn_fwd_kernel<D>;
+  const bool split = p.full_units != p.units;
+  auto kern = split ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = p.units < sms ? p.units : sms;
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  *launched = 1;
+  if (!split) return cudaSuccess;
+  // The merge is a programmatic dependent: its grid is set up while the forward grid drains,
+  // and griddepcontrol.wait orders its reads after the forward kernel's writes.
+  const long long rows = static_cast<long long>(p.units - p.full_units) * 256;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, attn_fwd_merge_kernel<D>, p);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  if (err == cudaSuccess) *launched = 2;
+  return err;
 }
 
 cudaError_t launch_attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -591,8 +770,18 @@ static bool use_pair_kernel() {
 }
 
 // Returns cudaErrorInvalidValue if a tensor map cannot be built (e.g. driver entry point missing).
-static cudaError_t launch_attn_fwd_single(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                            int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+//
+// Schedule: the units run on min(units, CTAs) persistent CTAs in rounds. When a non-causal
+// call's units leave the last round partly filled (r of `grid` CTAs busy) and a workspace is
+// given, each of those r units is split along its key blocks into s = min(grid / r, blocks)
+// pieces that run side by side, and the merge kernel combines them: the last round then takes
+// about 1/s of a unit instead of a whole one (non-causal MHA B8 H12 T4096 d64: 1536 units on
+// 152 CTAs, 16 in the last round, split 9 ways). Causal units are ordered heaviest first and
+// the snake order already balances them, so they are never split.
+static cudaError_t launch_attn_fwd_single(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                          int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                                          void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                                          int* launched) {
   CUtensorMap mq, mk, mv;
   if (!encode_bf16_tile_map(&mq, q, d, Tq, B * Hq) || !encode_bf16_tile_map(&mk, k, d, Tk, B * Hkv) ||
       !encode_bf16_tile_map(&mv, v, d, Tk, B * Hkv))
@@ -615,17 +804,41 @@ static cudaError_t launch_attn_fwd_single(const void* q, const void* k, const vo
   // (the kernel forms round * gridDim.x + gridDim.x in int)
   if (units <= 0 || units > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
   p.units = static_cast<int>(units);
-  return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, stream) : launch_fwd_d<128>(mq, mk, mv, p, stream);
+  const int ctas = prefill_ctas();
+  if (ctas <= 0) return cudaErrorInvalidDevice;
+  const int grid = p.units < ctas ? p.units : ctas;
+  p.full_units = p.units;
+  p.split = 1;
+  p.part_o = nullptr;
+  p.part_lse2 = nullptr;
+  if (!p.causal && workspace != nullptr && grid < p.units) {
+    const int r = p.units % grid;
+    const int blocks = (Tk + 127) / 128;
+    const int s = r > 0 ? std::min(grid / r, blocks) : 1;
+    if (s >= 2 && workspace_bytes >= split_scratch_bytes(grid, d)) {
+      p.full_units = p.units - r;
+      p.split = s;
+      p.part_o = static_cast<float*>(workspace);
+      p.part_lse2 = p.part_o + static_cast<size_t>(grid) * 256 * d;
+    }
+  }
+  p.items = p.full_units + (p.units - p.full_units) * p.split;  // <= units + grid
+  return d == 64 ? launch_fwd_d<64>(mq, mk, mv, p, grid, stream, launched)
+                 : launch_fwd_d<128>(mq, mk, mv, p, grid, stream, launched);
 }
 
 cudaError_t launch_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                            int Hkv, int Tq, int Tk, int d, int causal, float scale, cudaStream_t stream) {
+                            int Hkv, int Tq, int Tk, int d, int causal, float scale, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream, int* launched) {
+  *launched = 0;
   if (use_pair_kernel()) {
     const cudaError_t err = launch_attn_fwd_pair(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
+    if (err == cudaSuccess) *launched = 1;
     if (err != cudaErrorInvalidDevice) return err;
     (void)cudaGetLastError();  // no resident pair on this device: the single-CTA kernel runs
   }
-  return launch_attn_fwd_single(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream);
+  return launch_attn_fwd_single(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, workspace, workspace_bytes,
+                                stream, launched);
 }
 
 uint32_t prefill_take_device_error() { return take_device_error_word(); }

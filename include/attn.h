@@ -76,6 +76,43 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, cudaStream_t stream);
 
 /*
+ * attn_fwd_workspace_size - bytes of scratch attn_fwd_ws can use on the current
+ * device for head dimension d: 256 rows x (d + 1) fp32 values per streaming
+ * multiprocessor. Returns 0 when d is not 64 or 128.
+ */
+size_t attn_fwd_workspace_size(int d);
+
+/*
+ * attn_fwd_ws - attn_fwd with a scratch buffer, which lets a non-causal call
+ * balance its last round of work.
+ *
+ * The forward kernel runs its work units (two 128-row query tiles that share
+ * one K/V stream) on persistent thread blocks, one per SM, in rounds. When a
+ * non-causal call leaves the last round partly filled, the units of that round
+ * are split along the keys into pieces that run side by side. Each piece keeps
+ * its own (m, l, O), and a second kernel merges them in a fixed order with the
+ * online-softmax rescaling of "Module 07: Fused operators and FlashAttention",
+ * section "Online softmax: derivation" (the merge flash-decoding uses; "Attention
+ * from the kernel's side", section "Prefill and decoding are different
+ * problems"). Causal calls are never split. The rows of the split units agree
+ * with attn_fwd to rounding, not bit for bit; every other row is identical.
+ *
+ *   workspace        device memory of at least attn_fwd_workspace_size(d)
+ *                    bytes, 16-byte aligned, owned by the caller and not read
+ *                    or written by anything else until the call's work on
+ *                    `stream` has finished; or NULL with workspace_bytes 0,
+ *                    which makes the call exactly attn_fwd.
+ *   everything else  as attn_fwd.
+ * Errors: as attn_fwd; ATTN_ERR_WORKSPACE when workspace is NULL with a non-zero
+ * size or smaller than attn_fwd_workspace_size(d); ATTN_ERR_MISALIGNED when it
+ * is not 16-byte aligned.
+ */
+attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                        int causal, float scale, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/*
  * attn_decode_workspace_size - bytes of scratch attn_decode needs.
  * Returns 0 for invalid arguments. The workspace holds one fp32 partial
  * (m, l, o[d]) per (sequence, query head, split).
