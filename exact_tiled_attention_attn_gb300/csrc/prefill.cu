@@ -41,6 +41,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -619,9 +620,11 @@ __global__ void __launch_bounds__(352, 1)
 // One warp per query row of a split unit: lane p reads piece p's log-sum-exp (32 pieces at a
 // time), the maximum and the weights' sum are reduced across the warp (a fixed tree), and the
 // weighted sum of the pieces' rows runs in piece order with lane e holding D/32 consecutive
-// columns, its loads unrolled so that several pieces' rows are in flight at once (the kernel
-// is bound by load latency, not bandwidth). Launched as a programmatic dependent of the
-// prefill kernel.
+// columns. Up to kMergeBatch pieces, every load of the row is issued before the first is used
+// (the kernel is bound by load latency, not bandwidth). Launched as a programmatic dependent
+// of the prefill kernel.
+constexpr int kMergeBatch = 16;  // pieces whose rows one warp loads at once
+
 template <int D>
 __global__ void __launch_bounds__(256) attn_fwd_merge_kernel(const PrefillParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the pieces' results are complete
@@ -633,47 +636,63 @@ __global__ void __launch_bounds__(256) attn_fwd_merge_kernel(const PrefillParams
   const int i = wg & 127;
   if (t >= p.units - p.full_units) return;
   const UnitInfo u = decode_unit(p, p.full_units + t);
-  const int row = u.row0[q] + i;
-  if (u.nkv[q] == 0 || row >= p.Tq) return;
+  const int row = (q ? u.row0[1] : u.row0[0]) + i;  // selects, not a runtime index into u
+  const int head = q ? u.head[1] : u.head[0];
+  if ((q ? u.nkv[1] : u.nkv[0]) == 0 || row >= p.Tq) return;
   // piece pc of unit t is part t * split + pc: its row i of tile q is at ((part * 2 + q) * 128 + i)
   const size_t row_p0 = (static_cast<size_t>(t) * p.split * 2 + q) * 128 + i;
   const float* lse2 = p.part_lse2 + row_p0;
-  float mx = -INFINITY;
-  for (int c = 0; c < p.split; c += 32)
-    if (c + lane < p.split) mx = fmaxf(mx, lse2[static_cast<size_t>(c + lane) * 256]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  const float* src = p.part_o + row_p0 * D + lane * E;
+  using VecE = typename std::conditional<E == 2, float2, float4>::type;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int c = 0; c < p.split; c += 32) {
-    const int n = min(32, p.split - c);
-    const float w_lane = lane < n ? ex2_approx(lse2[static_cast<size_t>(c + lane) * 256] - mx) : 0.f;
-    float ws = w_lane;
+  float mx = -INFINITY, wsum = 0.f;
+  auto fma_row = [&](float w, const VecE& x) {
+    acc[0] = fmaf(w, x.x, acc[0]);
+    acc[1] = fmaf(w, x.y, acc[1]);
+    if constexpr (E == 4) {
+      acc[2] = fmaf(w, reinterpret_cast<const float4&>(x).z, acc[2]);
+      acc[3] = fmaf(w, reinterpret_cast<const float4&>(x).w, acc[3]);
+    }
+  };
+  if (p.split <= kMergeBatch) {
+    // every load issued before any is used: one memory latency for the whole row
+    const float l_lane = lane < p.split ? lse2[static_cast<size_t>(lane) * 256] : -INFINITY;
+    VecE x[kMergeBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
-    wsum += ws;
-    const float* src = p.part_o + (row_p0 + static_cast<size_t>(c) * 256) * D + lane * E;
+    for (int pc = 0; pc < kMergeBatch; ++pc)
+      if (pc < p.split) x[pc] = *reinterpret_cast<const VecE*>(src + static_cast<size_t>(pc) * 256 * D);
+    mx = l_lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const float w_lane = lane < p.split ? ex2_approx(l_lane - mx) : 0.f;
+    wsum = w_lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+#pragma unroll
+    for (int pc = 0; pc < kMergeBatch; ++pc)
+      if (pc < p.split) fma_row(__shfl_sync(0xFFFFFFFFu, w_lane, pc), x[pc]);
+  } else {
+    for (int c = 0; c < p.split; c += 32)
+      if (c + lane < p.split) mx = fmaxf(mx, lse2[static_cast<size_t>(c + lane) * 256]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    for (int c = 0; c < p.split; c += 32) {
+      const int n = min(32, p.split - c);
+      const float w_lane = lane < n ? ex2_approx(lse2[static_cast<size_t>(c + lane) * 256] - mx) : 0.f;
+      float ws = w_lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
+      wsum += ws;
 #pragma unroll 4
-    for (int pc = 0; pc < n; ++pc) {
-      const float w = __shfl_sync(0xFFFFFFFFu, w_lane, pc);
-      const float* r = src + static_cast<size_t>(pc) * 256 * D;
-      if constexpr (E == 2) {
-        const float2 x = *reinterpret_cast<const float2*>(r);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-      } else {
-        const float4 x = *reinterpret_cast<const float4*>(r);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]);
-        acc[3] = fmaf(w, x.w, acc[3]);
-      }
+      for (int pc = 0; pc < n; ++pc)
+        fma_row(__shfl_sync(0xFFFFFFFFu, w_lane, pc),
+                *reinterpret_cast<const VecE*>(src + static_cast<size_t>(c + pc) * 256 * D));
     }
   }
   const float inv = 1.f / wsum;
-  const size_t orow = (static_cast<size_t>(u.b) * p.Hq + u.head[q]) * p.Tq + row;
+  const size_t orow = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row;
   __nv_bfloat16* dst = p.o + orow * D + lane * E;
   if constexpr (E == 2) {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);

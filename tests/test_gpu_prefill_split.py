@@ -76,6 +76,8 @@ CASES = [
     (1, 2, 2, 1100, 1100, 128, 4),    # 10 units; the split ones hold an inactive second tile
     (1, 2, 1, 300, 2000, 128, 2),     # Tq < Tk: 3 units, 1 split in 2 pieces of 8 blocks
     (3, 6, 2, 384, 700, 64, 8),       # g = 3 row tiles, 36 units: 4 split in 2
+    (1, 2, 2, 5376, 2600, 64, 40),    # 42 units: 2 split in 20 (more pieces than one merge batch)
+    (36, 1, 1, 256, 4480, 128, 35),   # 36 units: 1 split in 35 (more pieces than a warp's lanes)
 ]
 
 
