@@ -46,8 +46,8 @@ WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 # ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md, with
 # the SHA-256 of the kernel's sources (prefill.cu and common.cuh) it was taken with: the figure is
 # reported only while those sources are unchanged.
-PREFILL_TRAFFIC = {"bytes": 350143488 + 94693888,
-                   "sources_sha256": "c9dfee36afc563e2a79d2d0ff67479b6cb1d88348d5d78cf625145fbc8c98617"}
+PREFILL_TRAFFIC = {"bytes": 280165120 + 82476032,
+                   "sources_sha256": "88f300b8b0a17a771c97a3efc52f7827787428f52abc572236f987e2eab2afeb"}
 PREFILL_SOURCES = ("prefill.cu", "common.cuh")
 
 
