@@ -33,6 +33,11 @@
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_q aliases the first 64 columns of S_q.
 //
+// Work distribution: one persistent CTA per SM walks the units in rounds (snake order,
+// heaviest first when causal). A non-causal launch whose last round would be only partly
+// filled runs that round's units as pieces over consecutive key blocks instead, and
+// attn_fwd_merge_kernel combines each unit's pieces (the online-softmax merge).
+//
 // The maximum used as the exponent base is only moved when the new block maximum
 // exceeds it by more than 2^8 (in base 2); the normalised result does not depend on
 // which finite base is subtracted ("Module 07", section "Online softmax: derivation":
@@ -85,6 +90,7 @@ struct PrefillParams {
   int pair_heads;  // 1: tiles are heads (2p, 2p+1) at the same rows; 0: row tiles (2p, 2p+1) of one head
   int n_qt;        // number of query tiles of 128 rows
   int units;       // work units (pairs of query tiles), heaviest first when causal
+  int rank_div, rank_mod, rest_div, rest_mod;  // unit -> (row-tile rank, batch-head rest); decode_unit
   // Key-split tail (see decode_item): units [0, full_units) run whole; each later unit runs as
   // `split` pieces over consecutive ranges of its key blocks, whose partial results go to
   // part_o / part_lse2 and are merged by attn_fwd_merge_kernel. items = the work items.
@@ -111,13 +117,18 @@ __device__ __forceinline__ int kv_tiles_for(const PrefillParams& p, int row0) {
   return min(all, last_row / 128 + 1);
 }
 
+// Unit order. Causal: by query-tile rank, heaviest (last rows) first, then (batch, head), so
+// that the snake order balances the CTAs. Non-causal (all units equally long): (batch, head)
+// major and the row tile fastest, so that the units running at one time cover few heads and
+// their K/V blocks are read from L2 rather than DRAM.
 __device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit) {
   UnitInfo u;
+  // rank = (unit / rank_div) % rank_mod and rest = (unit / rest_div) % rest_mod, with the
+  // divisors set on the host for the order above (no branch: fewer live registers)
+  const int rank = (unit / p.rank_div) % p.rank_mod;
+  const int rest = (unit / p.rest_div) % p.rest_mod;
   if (p.pair_heads) {
     const int hp_count = p.Hq / 2;
-    const int per_rank = hp_count * p.B;
-    const int rank = unit / per_rank;
-    const int rest = unit % per_rank;
     const int hp = rest % hp_count;
     u.b = rest / hp_count;
     const int qt = p.causal ? (p.n_qt - 1 - rank) : rank;  // heaviest tiles first when causal
@@ -126,9 +137,6 @@ __device__ __forceinline__ UnitInfo decode_unit(const PrefillParams& p, int unit
     u.row0[0] = u.row0[1] = qt * 128;
   } else {
     const int n_pairs = (p.n_qt + 1) / 2;
-    const int per_rank = p.Hq * p.B;
-    const int rank = unit / per_rank;
-    const int rest = unit % per_rank;
     const int h = rest % p.Hq;
     u.b = rest / p.Hq;
     const int tp = p.causal ? (n_pairs - 1 - rank) : rank;
@@ -823,6 +831,20 @@ static cudaError_t launch_attn_fwd_single(const void* q, const void* k, const vo
   // (the kernel forms round * gridDim.x + gridDim.x in int)
   if (units <= 0 || units > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
   p.units = static_cast<int>(units);
+  // unit order (decode_unit): causal rank-major, non-causal (batch, head)-major
+  const int ranks = p.pair_heads ? p.n_qt : (p.n_qt + 1) / 2;
+  const int rests = p.units / ranks;
+  if (p.causal) {
+    p.rank_div = rests;
+    p.rank_mod = ranks;
+    p.rest_div = 1;
+    p.rest_mod = rests;
+  } else {
+    p.rank_div = 1;
+    p.rank_mod = ranks;
+    p.rest_div = ranks;
+    p.rest_mod = rests;
+  }
   const int ctas = prefill_ctas();
   if (ctas <= 0) return cudaErrorInvalidDevice;
   const int grid = p.units < ctas ? p.units : ctas;

@@ -45,16 +45,15 @@ def split_plan(B, Hq, Hkv, Tq, Tk, ctas, causal):
 
 
 def unit_rows(B, Hq, Hkv, Tq, unit):
-    """(b, head, first row) of the two tiles of a unit, in the kernel's unit order (non-causal)."""
+    """(b, head, first row) of the two tiles of a unit, in the kernel's non-causal unit order:
+    (batch, head) major, the row tile fastest."""
     n_qt = (Tq + 127) // 128
     g = Hq // Hkv
     if g % 2 == 0:
-        per_rank = (Hq // 2) * B
-        rank, rest = divmod(unit, per_rank)
+        rest, rank = divmod(unit, n_qt)
         b, hp = divmod(rest, Hq // 2)
         return [(b, 2 * hp, rank * 128), (b, 2 * hp + 1, rank * 128)]
-    per_rank = Hq * B
-    rank, rest = divmod(unit, per_rank)
+    rest, rank = divmod(unit, (n_qt + 1) // 2)
     b, h = divmod(rest, Hq)
     return [(b, h, 2 * rank * 128), (b, h, (2 * rank + 1) * 128)]
 
@@ -157,8 +156,8 @@ def test_workspace_arguments_are_checked(attn):
 
 def test_full_size_mha_tail_rows(attn):
     """Non-causal MHA B8 H12 T4096 d64 on every SM: the last round's units are split; their
-    rows (the last 256 rows of the last heads) against the oracle, and the rest bitwise equal
-    to the unsplit kernel."""
+    rows (all row tiles of the last head) against the oracle, and the rest bitwise equal to
+    the unsplit kernel."""
     shp = W.MHA_GPT2
     q, k, v = W.attention_inputs(shp)[:3]
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
