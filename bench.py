@@ -76,6 +76,13 @@ def _peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def decode_kernels(splits: int, eb: int) -> str:
+    cache = " (E4M3 cache)" if eb == 1 else ""
+    if splits == 0:
+        return f"decode_balanced_kernel<128,{eb}>{cache} + decode_balanced_merge_kernel<128>"
+    return f"decode_split_mma_kernel<128,{eb}>{cache} + decode_combine_kernel<128>"
+
+
 # ----------------------------------------------------------------------------- clocks
 
 def summarise_clock_samples(samples, t0: float, t1: float, source: str):
@@ -284,7 +291,9 @@ def run_gpu(args):
     dq, dkc, dvc, dsl = W.decode_inputs(DECODE)
     dqd, dkcd, dvcd, dsld = dq.to(dev), dkc.to(dev), dvc.to(dev), dsl.to(dev)
     del dkc, dvc
-    splits = args.splits or attn.default_splits(DECODE.B, DECODE.Hkv, DECODE.Lcap)
+    # 0 = the balanced schedule (equal key ranges over persistent CTAs, then a merge of the cut
+    # segments); N >= 1 = flash-decoding with N splits per sequence
+    splits = args.splits if args.splits is not None else 0
     ws = torch.empty(attn.decode_workspace_size(DECODE.B, DECODE.Hq, DECODE.d, splits), dtype=torch.uint8,
                      device=dev)
     dod = torch.empty_like(dqd)
@@ -586,6 +595,22 @@ def run_gpu(args):
                                       "GB/s": round(r_bytes / (r_ms * 1e-3) / 1e9, 1),
                                       "timing": "one launch between two events, L2 flushed before it"}}
 
+    # ---- the bf16 decode of the step, 20 launches back to back (consecutive decode steps of a
+    #      serving loop; the in-step number above follows the prefill, whose writes are still
+    #      in L2)
+    nb = 20
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(nb):
+        attn.decode(dqd, dkcd, dvcd, dsld, scale=DECODE.scale, num_splits=splits, workspace=ws, out=dod, lse=dlse)
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    db_ms = max_over_ranks([a.elapsed_time(b) / nb], dev)[0]
+    dec_b2b = {"value": round(dec_bytes / (db_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "frac": round(dec_bytes / (db_ms * 1e-3) / 1e9 / peaks["hbm"], 4), "ms": round(db_ms, 4),
+               "timing": f"{nb} launches back to back between two events"}
+
     # ---- FP8 (E4M3) KV-cache decode on the same workload (its own timing, outside the step):
     #      the cache is quantised once on the GPU, then only the 1-byte codes are streamed
     dec8 = None
@@ -612,7 +637,8 @@ def run_gpu(args):
         dec8 = {"value": round(d8_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                 "frac": round(d8_gbs / peaks["hbm"], 4), "ms": round(d8_ms, 4), "bytes_per_launch": d8_bytes,
                 "vs_bf16_decode_time": round(dec_ms / d8_ms, 3),
-                "kernels": "decode_split_mma_kernel<128,1> (E4M3 cache) + decode_combine_kernel<128>",
+                "kernels": decode_kernels(splits, 1),
+                "timing": f"{n8} launches back to back between two events",
                 "num_splits": splits}
         del kq, vq
 
@@ -731,8 +757,10 @@ def run_gpu(args):
                          "flops_per_launch": flops},
             "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                        "frac": round(dec_gbs / peaks["hbm"], 4), "bytes_per_launch": dec_bytes,
-                       "kernels": "decode_split_mma_kernel<128,2> + decode_combine_kernel<128>",
-                       "num_splits": splits},
+                       "kernels": decode_kernels(splits, 2),
+                       "num_splits": splits,
+                       "timing": "one launch inside the step, after the prefill (between two events)",
+                       "back_to_back": dec_b2b},
             "rmsnorm": {"value": norm_graph["GB/s"], "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm"],
                         "frac": norm_graph["frac"], "bytes_per_launch": norm_bytes,
                         "timing": "a kernel this short is timed as a CUDA graph of back-to-back launches over "
@@ -866,7 +894,8 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = library default)")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="decode split count; 0 (the default) = the balanced schedule")
     ap.add_argument("--cpu-heads", type=int, default=8, help="(batch, head) pairs in the CPU-baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="approximate oracle time of a whole --impl reference run")

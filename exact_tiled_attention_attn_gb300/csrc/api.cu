@@ -21,6 +21,8 @@ cudaError_t launch_rmsnorm(const void* x, const void* r, const void* w, void* y,
                            cudaStream_t s);
 int rmsnorm_segments(int D);
 size_t decode_noalloc_capacity();
+size_t decode_balanced_workspace_bytes(int d);
+int decode_balanced_max_batch();
 cudaError_t decode_noalloc_scratch(cudaStream_t stream, void** ptr);
 cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Tq, int Tk,
@@ -44,7 +46,8 @@ static attn_status check_decode_args(const void* q, const void* kcache, const vo
   if (B < 1 || Hq < 1 || Hkv < 1 || Lcap < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (num_splits < 1 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
+  // 0 selects the balanced schedule; otherwise splits of at least 16 keys
+  if (num_splits < 0 || num_splits > (Lcap + 15) / 16) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
@@ -52,10 +55,19 @@ static attn_status check_decode_args(const void* q, const void* kcache, const vo
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
   if (static_cast<long long>(num_splits) > 65535 || static_cast<long long>(Hkv) > 65535 || B > 65535)
     return ATTN_ERR_UNSUPPORTED;
+  if (num_splits == 0) {
+    // the balanced schedule keeps the tile prefix sums of all sequences in shared memory and
+    // counts tiles (64 keys) of all (sequence, head block) segments in an int
+    const long long blocks = (Hq / Hkv + 3) / 4;  // head blocks per K/V head
+    if (B > decode_balanced_max_batch()) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(Hkv) * blocks * B * ((static_cast<long long>(Lcap) + 63) / 64) >= 0x7FFFFFFFLL)
+      return ATTN_ERR_UNSUPPORTED;
+  }
   return ATTN_OK;
 }
 
 static int decode_chunk(int Lcap, int num_splits) {
+  if (num_splits == 0) return 0;  // balanced schedule: no fixed chunks
   const long long c = (static_cast<long long>(Lcap) + num_splits - 1) / num_splits;
   return static_cast<int>((c + 15) / 16 * 16);
 }
@@ -117,7 +129,8 @@ attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, fl
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
-  if (B < 1 || Hq < 1 || d < 1 || num_splits < 1) return 0;
+  if (B < 1 || Hq < 1 || d < 1 || num_splits < 0) return 0;
+  if (num_splits == 0) return (d == 64 || d == 128) ? decode_balanced_workspace_bytes(d) : 0;
   return static_cast<size_t>(B) * Hq * num_splits * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 

@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB>::kThreads, 3)
 __device__ __forceinline__ void mma_16816_bf16(float (&d)[2], const uint32_t a0, const uint32_t a2, uint32_t b0,
                                                uint32_t b1) {
   // rows 8..15 of A are zero, so d2 and d3 stay zero: they are not kept
-  float z2, z3;  // NOLINT: outputs of the instruction, unused
+  [[maybe_unused]] float z2, z3;  // outputs of the instruction, unused
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %10, %10};"
@@ -459,7 +459,7 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[2], const uint32_t a0,
 }
 __device__ __forceinline__ void mma_16816_f16(float (&d)[2], const uint32_t a0, const uint32_t a2, uint32_t b0,
                                               uint32_t b1) {
-  float z2, z3;
+  [[maybe_unused]] float z2, z3;
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %10, %10};"
@@ -482,6 +482,149 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---- the tensor-core consumer's building blocks (shared by the split and balanced kernels)
+
+// Q of this thread's head (row gq of the MMA's A operand; a zero row when the CTA has fewer
+// heads) as A fragments: for MMA kk, the k-slots (2c, 2c+1) and (2c+8, 2c+9) hold the elements
+// QE c + 4 kk + (0, 1) and QE c + 4 kk + (2, 3) of the head's row (an E4M3 cache: as f16).
+template <int D, int EB>
+__device__ __forceinline__ void mma_load_q(const __nv_bfloat16* qrow_head, bool head_ok, int c,
+                                           uint32_t (&qa)[D / 16][2]) {
+  constexpr int QE = D / 4;
+  const uint4* qrow = reinterpret_cast<const uint4*>(qrow_head + QE * c);
+#pragma unroll
+  for (int i = 0; i < QE / 8; ++i) {
+    const uint4 v = qrow[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t x = head_ok ? w[e] : 0u;
+      if constexpr (EB == 1) x = pack_f16x2(bf16lo_to_f32(x), bf16hi_to_f32(x));
+      qa[(4 * i + e) >> 1][e & 1] = x;
+    }
+  }
+}
+
+// One consumer warp's block of 16 keys (rows of kt / vt, kRowBytes apart; rows at or past
+// nvalid are masked): S = Q K^T, the online-softmax update of (m, l) and O += P V.
+//  * S: key 8 nt + gq of the block is this thread's column; the d axis is permuted so that the
+//    thread's k-slots of every MMA lie in one contiguous quarter of its key row (the dot
+//    product does not depend on the order of its terms when Q and K use the same one).
+//  * The base only moves when a score exceeds it by more than 2^8; then the block maximum is
+//    formed (two xor shuffles within the 4 threads of a head).
+//  * O: B of MMA j holds V rows (2c, 2c+1) and (2c+8, 2c+9) of the block at output column
+//    VE gq + j; P is reused from the S accumulators (the FA-2 register reuse).
+template <int D, int EB, int kRowBytes>
+__device__ __forceinline__ void mma_decode_block(const uint8_t* kt, const uint8_t* vt, int nvalid,
+                                                 const uint32_t (&qa)[D / 16][2], float cmul, int gq, int c,
+                                                 float& m, float& l, float (&o)[D / 8][2]) {
+  constexpr int NJ = D / 8;
+  constexpr int QE = D / 4;
+  constexpr int KW = QE * EB / 4;
+  constexpr int VE = D / 8;
+  constexpr int VW = VE * EB / 4;
+  float sc[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const uint4* krow = reinterpret_cast<const uint4*>(kt + (8 * nt + gq) * kRowBytes + QE * EB * c);
+    float acc[2] = {0.f, 0.f};
+    // one 16-byte piece at a time: 2 MMAs of bf16, 4 of E4M3 codes
+#pragma unroll
+    for (int i = 0; i < KW / 4; ++i) {
+      const uint4 v = krow[i];
+      const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+      if constexpr (EB == 2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) mma_16816<EB>(acc, qa[2 * i + h][0], qa[2 * i + h][1], kw[2 * h], kw[2 * h + 1]);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          mma_16816<EB>(acc, qa[4 * i + h][0], qa[4 * i + h][1], e4m3x2_to_f16x2(kw[h]), e4m3x2_to_f16x2(kw[h] >> 16));
+      }
+    }
+    // keys 8 nt + 2c and 8 nt + 2c + 1 of the block, base-2 scaled; keys past the end: -inf
+    sc[nt][0] = (8 * nt + 2 * c < nvalid) ? acc[0] * cmul : -INFINITY;
+    sc[nt][1] = (8 * nt + 2 * c + 1 < nvalid) ? acc[1] * cmul : -INFINITY;
+  }
+
+  const float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+  float corr = 1.f;
+  if (__any_sync(0xFFFFFFFFu, mx > m + kDecodeRescaleThreshold)) {
+    float mt = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 2));
+    const float m_cand = fmaxf(m, mt);
+    if (m_cand > m + kDecodeRescaleThreshold) {
+      corr = ex2_approx(m - m_cand);  // 0 when m was -inf
+      m = m_cand;
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      o[j][0] *= corr;
+      o[j][1] *= corr;
+    }
+  }
+  const float base = (m == -INFINITY) ? 0.f : m;
+  float pw[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    pw[nt][0] = ex2_approx(sc[nt][0] - base);
+    pw[nt][1] = ex2_approx(sc[nt][1] - base);
+  }
+  l = l * corr + ((pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]));
+  const uint32_t pa0 = (EB == 2) ? pack_bf16x2(pw[0][0], pw[0][1]) : pack_f16x2(pw[0][0], pw[0][1]);
+  const uint32_t pa2 = (EB == 2) ? pack_bf16x2(pw[1][0], pw[1][1]) : pack_f16x2(pw[1][0], pw[1][1]);
+
+  // Rows past the end are zeroed (their shared memory may hold anything, and 0 * NaN would
+  // not be 0). In halves of the output columns (16-byte pieces of the four rows), to keep
+  // registers low.
+  constexpr int kHalves = (VW >= 8) ? 2 : 1;
+  constexpr int HW = VW / kHalves;  // 32-bit words of a row per half
+  constexpr int HJ = NJ / kHalves;  // MMAs per half
+#pragma unroll
+  for (int hf = 0; hf < kHalves; ++hf) {
+    uint32_t vw[4][HW];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = 2 * c + (r & 1) + 8 * (r >> 1);
+      const bool ok = row < nvalid;
+      const uint8_t* vrow = vt + row * kRowBytes + VE * EB * gq + hf * HW * 4;
+      if constexpr (HW >= 4) {
+#pragma unroll
+        for (int i = 0; i < HW / 4; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(vrow + i * 16);
+          vw[r][4 * i] = ok ? v.x : 0u;
+          vw[r][4 * i + 1] = ok ? v.y : 0u;
+          vw[r][4 * i + 2] = ok ? v.z : 0u;
+          vw[r][4 * i + 3] = ok ? v.w : 0u;
+        }
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(vrow);
+        vw[r][0] = ok ? v.x : 0u;
+        vw[r][1] = ok ? v.y : 0u;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < HJ; ++jj) {
+      const int j = hf * HJ + jj;
+      uint32_t b0, b1;
+      if constexpr (EB == 2) {
+        // element j of rows (2c, 2c+1) into one register, likewise rows (2c+8, 2c+9)
+        const uint32_t sel = (jj & 1) ? 0x7632u : 0x5410u;
+        b0 = __byte_perm(vw[0][jj >> 1], vw[1][jj >> 1], sel);
+        b1 = __byte_perm(vw[2][jj >> 1], vw[3][jj >> 1], sel);
+      } else {
+        // codes j of rows (2c, 2c+1) -> one f16 pair, likewise rows (2c+8, 2c+9)
+        const uint32_t sel = (jj & 2) ? 0x7362u : 0x5140u;
+        const uint32_t w01 = __byte_perm(vw[0][jj >> 2], vw[1][jj >> 2], sel);
+        const uint32_t w23 = __byte_perm(vw[2][jj >> 2], vw[3][jj >> 2], sel);
+        b0 = e4m3x2_to_f16x2((jj & 1) ? (w01 >> 16) : w01);
+        b1 = e4m3x2_to_f16x2((jj & 1) ? (w23 >> 16) : w23);
+      }
+      mma_16816<EB>(o[j], pa0, pa2, b0, b1);
+    }
+  }
+}
+
 // Two CTAs per SM (at d = 128 this kernel needs ~168 registers per thread) and 3 stages of 64
 // rows, 6 for the 1-byte rows of an E4M3 cache at d = 128 (96 KB of K and V per CTA, as with
 // bf16 rows). Measured on the B16 Hq32 Hkv8 L ~ U[8192, 32768] decode: E4M3 d = 128, 6 stages
@@ -498,12 +641,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThread
     decode_split_mma_kernel(const DecodeParams p) {
   using Cfg = DecodeCfg<D, EB, mma_stages<D, EB>()>;
   static_assert(Cfg::kTile == 16 * Cfg::kConsumerWarps, "one 16-key block per consumer warp per stage");
-  constexpr int KK = D / 16;          // MMAs along d for S
   constexpr int NJ = D / 8;           // MMAs along the output columns for O
-  constexpr int QE = D / 4;           // elements of a key row one thread reads for S
-  constexpr int KW = QE * EB / 4;     // 32-bit words of them
-  constexpr int VE = D / 8;           // elements of a value row one thread reads for O
-  constexpr int VW = VE * EB / 4;     // 32-bit words of them
+  constexpr int VE = D / 8;           // elements of a value row one thread holds per output MMA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
@@ -569,24 +708,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThread
   const int gq = lane >> 2;  // MMA row group: the query head (rows of A, P, O); the key / column of B
   const int c = lane & 3;    // position in the group
   const bool head_ok = gq < nh;
-  // Q as the A operand of S: for MMA kk, this thread's k-slots (2c, 2c+1) and (2c+8, 2c+9) hold
-  // the elements QE c + 4 kk + (0, 1) and QE c + 4 kk + (2, 3) of its head's row
-  uint32_t qa[KK][2];
-  {
-    const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * p.Hq + (head_ok ? h0 + gq : h0)) * D +
-                                                       QE * c);
-#pragma unroll
-    for (int i = 0; i < QE / 8; ++i) {
-      const uint4 v = qrow[i];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint32_t x = head_ok ? w[e] : 0u;
-        if constexpr (EB == 1) x = pack_f16x2(bf16lo_to_f32(x), bf16hi_to_f32(x));
-        qa[(4 * i + e) >> 1][e & 1] = x;
-      }
-    }
-  }
+  uint32_t qa[D / 16][2];
+  mma_load_q<D, EB>(p.q + (static_cast<size_t>(b) * p.Hq + (head_ok ? h0 + gq : h0)) * D, head_ok, c, qa);
   const float cmul = p.c * (p.k_scale != nullptr ? p.k_scale[static_cast<size_t>(b) * p.Hkv + kvh] : 1.f);
   float m = -INFINITY, l = 0.f;
   float o[NJ][2];
@@ -600,113 +723,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThread
     const uint8_t* kt = sK + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
     const uint8_t* vt = sV + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
     const int key0 = start + t * Cfg::kTile + warp * 16;  // first key of this warp's block
-    const int nvalid = end - key0;                        // keys of the block inside the split (may be <= 0)
-
-    // ---- S = Q K^T for the block's two groups of 8 keys (key 8 nt + gq of the block is this
-    //      thread's column)
-    float sc[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const uint4* krow = reinterpret_cast<const uint4*>(kt + (8 * nt + gq) * Cfg::kRowBytes + QE * EB * c);
-      float acc[2] = {0.f, 0.f};
-      // one 16-byte piece at a time: 2 MMAs of bf16, 4 of E4M3 codes
-#pragma unroll
-      for (int i = 0; i < KW / 4; ++i) {
-        const uint4 v = krow[i];
-        const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
-        if constexpr (EB == 2) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) mma_16816<EB>(acc, qa[2 * i + h][0], qa[2 * i + h][1], kw[2 * h], kw[2 * h + 1]);
-        } else {
-#pragma unroll
-          for (int h = 0; h < 4; ++h)
-            mma_16816<EB>(acc, qa[4 * i + h][0], qa[4 * i + h][1], e4m3x2_to_f16x2(kw[h]), e4m3x2_to_f16x2(kw[h] >> 16));
-        }
-      }
-      // keys 8 nt + 2c and 8 nt + 2c + 1 of the block, base-2 scaled; keys past the split end: -inf
-      sc[nt][0] = (8 * nt + 2 * c < nvalid) ? acc[0] * cmul : -INFINITY;
-      sc[nt][1] = (8 * nt + 2 * c + 1 < nvalid) ? acc[1] * cmul : -INFINITY;
-    }
-
-    // ---- online softmax per head (row gq; the 4 threads of a group share it). The base only
-    //      moves when a score exceeds it by more than 2^8; then the block maximum is formed.
-    const float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    float corr = 1.f;
-    if (__any_sync(0xFFFFFFFFu, mx > m + kDecodeRescaleThreshold)) {
-      float mt = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 2));
-      const float m_cand = fmaxf(m, mt);
-      if (m_cand > m + kDecodeRescaleThreshold) {
-        corr = ex2_approx(m - m_cand);  // 0 when m was -inf
-        m = m_cand;
-      }
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) {
-        o[j][0] *= corr;
-        o[j][1] *= corr;
-      }
-    }
-    const float base = (m == -INFINITY) ? 0.f : m;
-    float pw[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      pw[nt][0] = ex2_approx(sc[nt][0] - base);
-      pw[nt][1] = ex2_approx(sc[nt][1] - base);
-    }
-    l = l * corr + ((pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]));
-    const uint32_t pa0 = (EB == 2) ? pack_bf16x2(pw[0][0], pw[0][1]) : pack_f16x2(pw[0][0], pw[0][1]);
-    const uint32_t pa2 = (EB == 2) ? pack_bf16x2(pw[1][0], pw[1][1]) : pack_f16x2(pw[1][0], pw[1][1]);
-
-    // ---- O += P V: B of MMA j holds V rows (2c, 2c+1) and (2c+8, 2c+9) of the block at output
-    //      column VE gq + j. Rows past the split end are zeroed (their shared memory may hold
-    //      anything, and 0 * NaN would not be 0).
-    // in halves of the output columns (16-byte pieces of the four rows), to keep registers low
-    constexpr int kHalves = (VW >= 8) ? 2 : 1;
-    constexpr int HW = VW / kHalves;  // 32-bit words of a row per half
-    constexpr int HJ = NJ / kHalves;  // MMAs per half
-#pragma unroll
-    for (int hf = 0; hf < kHalves; ++hf) {
-      uint32_t vw[4][HW];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int row = 2 * c + (r & 1) + 8 * (r >> 1);
-        const bool ok = row < nvalid;
-        const uint8_t* vrow = vt + row * Cfg::kRowBytes + VE * EB * gq + hf * HW * 4;
-        if constexpr (HW >= 4) {
-#pragma unroll
-          for (int i = 0; i < HW / 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(vrow + i * 16);
-            vw[r][4 * i] = ok ? v.x : 0u;
-            vw[r][4 * i + 1] = ok ? v.y : 0u;
-            vw[r][4 * i + 2] = ok ? v.z : 0u;
-            vw[r][4 * i + 3] = ok ? v.w : 0u;
-          }
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(vrow);
-          vw[r][0] = ok ? v.x : 0u;
-          vw[r][1] = ok ? v.y : 0u;
-        }
-      }
-#pragma unroll
-      for (int jj = 0; jj < HJ; ++jj) {
-        const int j = hf * HJ + jj;
-        uint32_t b0, b1;
-        if constexpr (EB == 2) {
-          // element j of rows (2c, 2c+1) into one register, likewise rows (2c+8, 2c+9)
-          const uint32_t sel = (jj & 1) ? 0x7632u : 0x5410u;
-          b0 = __byte_perm(vw[0][jj >> 1], vw[1][jj >> 1], sel);
-          b1 = __byte_perm(vw[2][jj >> 1], vw[3][jj >> 1], sel);
-        } else {
-          // codes j of rows (2c, 2c+1) -> one f16 pair, likewise rows (2c+8, 2c+9)
-          const uint32_t sel = (jj & 2) ? 0x7362u : 0x5140u;
-          const uint32_t w01 = __byte_perm(vw[0][jj >> 2], vw[1][jj >> 2], sel);
-          const uint32_t w23 = __byte_perm(vw[2][jj >> 2], vw[3][jj >> 2], sel);
-          b0 = e4m3x2_to_f16x2((jj & 1) ? (w01 >> 16) : w01);
-          b1 = e4m3x2_to_f16x2((jj & 1) ? (w23 >> 16) : w23);
-        }
-        mma_16816<EB>(o[j], pa0, pa2, b0, b1);
-      }
-    }
+    mma_decode_block<D, EB, Cfg::kRowBytes>(kt, vt, end - key0, qa, cmul, gq, c, m, l, o);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[s]);
   }
@@ -759,6 +776,405 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThread
   }
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// ---------------------------------------------------------------------------------------
+// Balanced schedule (num_splits = 0).
+//
+// The split kernel gives every (split, head block, sequence) a CTA of its own. With
+// sequences of different lengths the CTAs differ in work, and the last ones run on a few SMs
+// while the others idle (globaltimer traces of every CTA: B16 Hq32 Hkv8 d128 with
+// L ~ U[8192, 32768] and 32 splits, the SMs fell idle from 184 us on and the kernel ended at
+// 205 us; with L ~ U[1024, 2048] and 2 splits it ended at 26 us against 15 us of average work
+// per SM). Here a persistent grid of kMmaCtasPerSm CTAs per SM divides the concatenated key
+// stream of all (sequence, head block) segments, in 64-key tiles, into equal ranges, one per
+// CTA (a stream-K partition: CTA c takes tiles [c NT / G, (c + 1) NT / G)). A CTA walks the
+// pieces of its range in order: a segment that lies wholly in the range is finished there
+// (O and LSE written, as the flash-decoding merge of one split); a segment cut by a range
+// boundary leaves one partial (m, l, o) per piece in the workspace, which the merge kernel
+// combines. Only a CTA's first piece can start inside a segment and only its last can end
+// inside one, so each CTA needs two partial slots: slot 2c for a piece that ends inside its
+// segment, slot 2c + 1 for one that starts inside its segment and runs to the end.
+// ---------------------------------------------------------------------------------------
+constexpr int kBalancedMaxB = 1024;  // sequences whose tile prefix sums fit the CTA's shared array
+
+struct BalancedParams {
+  const __nv_bfloat16* q;
+  const uint8_t* kc;  // [B, Hkv, Lcap, D] elements of EB bytes
+  const uint8_t* vc;
+  const float* k_scale;  // [B, Hkv] scales of an E4M3 cache (nullptr for bf16)
+  const float* v_scale;
+  const int* seqlens;
+  __nv_bfloat16* o;  // [B, Hq, D]
+  float* lse;        // [B, Hq] or nullptr
+  float* part;       // [2 G slots][kDecodeMaxHeadsPerCta heads][D + 2]: o, then m and l
+  int B, Hq, Hkv, g, n_hblk, hblk, Lcap;
+  int Y;             // segments per sequence: Hkv * n_hblk (head blocks)
+  int G;             // CTAs of the balanced kernel
+  float c;           // scale * log2(e)
+};
+
+__device__ __forceinline__ int seq_len_clamped(const int* seqlens, int b, int Lcap) {
+  const int L = seqlens[b];
+  return L < 0 ? 0 : (L > Lcap ? Lcap : L);
+}
+
+// The partition of the NT tiles over the CTAs: equal ranges over Geff = min(G, NT) CTAs, so
+// that none below Geff is empty (floor(c NT / Geff) strictly increases when NT >= Geff); CTAs
+// from Geff on have no work, and no empty range lies between two CTAs that share a segment.
+// (A second phase of smaller ranges for CTAs started later, meant to absorb the CTAs' speed
+// differences, was slower: the GPU does not start a grid's CTAs in index order, so some
+// large-range CTAs started after small ones; B16 Hq32 Hkv8 d128, L ~ U[8192, 32768]: 242 us
+// against 183 us back to back.)
+struct BalancedPartition {
+  int NT, Geff;
+  __device__ __forceinline__ BalancedPartition(int nt, int g) : NT(nt), Geff(nt < g ? nt : g) {}
+  // tiles [lo, hi) of CTA c (lo == hi: no work)
+  __device__ __forceinline__ void range(int c, int& lo, int& hi) const {
+    lo = hi = 0;
+    if (c < Geff) {
+      lo = static_cast<int>(static_cast<long long>(c) * NT / Geff);
+      hi = static_cast<int>(static_cast<long long>(c + 1) * NT / Geff);
+    }
+  }
+  // the CTA whose range holds tile t (0 <= t < NT): the largest c with floor(c NT / Geff) <= t
+  __device__ __forceinline__ int cta_of(int t) const {
+    return static_cast<int>((static_cast<long long>(t + 1) * Geff + NT - 1) / NT - 1);
+  }
+};
+
+// pre[b] = tiles of sequences 0..b-1 (pre[0] = 0), for b = 0..B, in shared memory; every
+// thread of the CTA takes part. Tiles are of kTile keys.
+template <int kTile>
+__device__ __forceinline__ void balanced_prefix(const BalancedParams& p, int* pre) {
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x)
+    pre[b + 1] = (seq_len_clamped(p.seqlens, b, p.Lcap) + kTile - 1) / kTile;
+  if (threadIdx.x == 0) pre[0] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {  // inclusive scan of pre[1..B] by warp 0, 32 entries at a time
+    int carry = 0;
+    for (int b0 = 1; b0 <= p.B; b0 += 32) {
+      const int i = b0 + static_cast<int>(threadIdx.x);
+      int v = i <= p.B ? pre[i] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
+        if (static_cast<int>(threadIdx.x) >= off) v += u;
+      }
+      if (i <= p.B) pre[i] = v + carry;
+      carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// One piece of a CTA's range: tiles [t0, t1) of segment (b, y), which covers tiles
+// [seg0, seg0 + n) of the stream; the piece's first tile is tile t0 - seg0 of the segment.
+struct DecodePiece {
+  int t0, t1, seg0;
+  int b, y, n;
+};
+
+// The piece that starts at tile t (< NT) and ends at min(hi, end of t's segment).
+// (Tile indices fit in an int: the host checks Y * B * ceil(Lcap / 64) < 2^31.)
+__device__ __forceinline__ DecodePiece balanced_piece(const BalancedParams& p, const int* pre, int t, int hi) {
+  // the largest b with Y pre[b] <= t: its segment row holds t (sequences without tiles are skipped)
+  int lo_b = 0, hi_b = p.B;  // invariant: Y pre[lo_b] <= t < Y pre[hi_b]
+  while (hi_b - lo_b > 1) {
+    const int mid = (lo_b + hi_b) >> 1;
+    if (p.Y * pre[mid] <= t) lo_b = mid;
+    else hi_b = mid;
+  }
+  DecodePiece pc;
+  pc.b = lo_b;
+  pc.n = pre[lo_b + 1] - pre[lo_b];
+  const int row0 = p.Y * pre[lo_b];
+  pc.y = (t - row0) / pc.n;
+  pc.seg0 = row0 + pc.y * pc.n;
+  pc.t0 = t;
+  pc.t1 = min(hi, pc.seg0 + pc.n);
+  return pc;
+}
+
+template <int D, int EB>
+__global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThreads, kMmaCtasPerSm)
+    decode_balanced_kernel(const BalancedParams p) {
+  using Cfg = DecodeCfg<D, EB, mma_stages<D, EB>()>;
+  static_assert(Cfg::kTile == 16 * Cfg::kConsumerWarps, "one 16-key block per consumer warp per stage");
+  constexpr int NJ = D / 8;
+  constexpr int VE = D / 8;
+  constexpr int kRed = D + 2;  // reduction row: o, m, l
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + Cfg::kStages * Cfg::kTileBytes;
+  float* red = reinterpret_cast<float*>(smem + 2 * Cfg::kStages * Cfg::kTileBytes);  // [warps][4 heads][kRed]
+  __shared__ uint64_t full_bar[Cfg::kStages];
+  __shared__ uint64_t empty_bar[Cfg::kStages];
+  __shared__ int abort_flag;
+  __shared__ int pre[kBalancedMaxB + 1];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], Cfg::kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  // the previous kernel's writes (the cache, q, the lengths) are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  balanced_prefix<Cfg::kTile>(p, pre);  // ends with __syncthreads
+  volatile int* abort_p = &abort_flag;
+  int lo, hi;
+  BalancedPartition(p.Y * pre[p.B], p.G).range(static_cast<int>(blockIdx.x), lo, hi);
+
+  if (warp == Cfg::kConsumerWarps) {
+    // ---------------- producer: every tile of every piece, in order ----------------
+    if (lane == 0) {
+      int T = 0;  // tiles issued by this CTA
+      bool alive = true;
+      for (int t = lo; alive && t < hi;) {
+        const DecodePiece pc = balanced_piece(p, pre, t, hi);
+        const int L = seq_len_clamped(p.seqlens, pc.b, p.Lcap);
+        const int kvh = pc.y / p.n_hblk;
+        const size_t head_off = (static_cast<size_t>(pc.b) * p.Hkv + kvh) * p.Lcap;
+        const uint8_t* kbase = p.kc + head_off * Cfg::kRowBytes;
+        const uint8_t* vbase = p.vc + head_off * Cfg::kRowBytes;
+        for (int i = pc.t0; i < pc.t1; ++i, ++T) {
+          const int s = T % Cfg::kStages;
+          if (!mbar_wait(&empty_bar[s], (static_cast<uint32_t>(T / Cfg::kStages) & 1u) ^ 1u, abort_p,
+                         kDecodeWaitTimeoutNs)) {
+            alive = false;
+            break;
+          }
+          const int row0 = (i - pc.seg0) * Cfg::kTile;
+          const int nrows = min(Cfg::kTile, L - row0);
+          const uint32_t bytes = static_cast<uint32_t>(nrows) * Cfg::kRowBytes;
+          mbar_arrive_expect_tx(&full_bar[s], 2 * bytes);
+          bulk_copy_g2s(sK + s * Cfg::kTileBytes, kbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes,
+                        &full_bar[s]);
+          bulk_copy_g2s(sV + s * Cfg::kTileBytes, vbase + static_cast<size_t>(row0) * Cfg::kRowBytes, bytes,
+                        &full_bar[s]);
+        }
+        t = pc.t1;
+      }
+      // the last copies land before the CTA may exit
+      for (int u = max(0, T - Cfg::kStages); u < T; ++u)
+        mbar_wait(&full_bar[u % Cfg::kStages], static_cast<uint32_t>(u / Cfg::kStages) & 1u, abort_p,
+                  kDecodeWaitTimeoutNs);
+    }
+    __syncwarp();
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;");
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int gq = lane >> 2;  // MMA row group: the query head
+  const int c = lane & 3;
+  int T = 0;  // tiles consumed by this CTA
+  for (int t = lo; t < hi;) {
+    int ntl, rem;  // tiles of the piece; keys of the sequence from this warp's first key on
+    float cmul;
+    uint32_t qa[D / 16][2];
+    {
+      const DecodePiece pc = balanced_piece(p, pre, t, hi);
+      const int L = seq_len_clamped(p.seqlens, pc.b, p.Lcap);
+      const int kvh = pc.y / p.n_hblk;
+      const int h0 = kvh * p.g + (pc.y % p.n_hblk) * p.hblk;
+      const bool head_ok = gq < min(p.hblk, (kvh + 1) * p.g - h0);
+      mma_load_q<D, EB>(p.q + (static_cast<size_t>(pc.b) * p.Hq + (head_ok ? h0 + gq : h0)) * D, head_ok, c, qa);
+      cmul = p.c * (p.k_scale != nullptr ? p.k_scale[static_cast<size_t>(pc.b) * p.Hkv + kvh] : 1.f);
+      ntl = pc.t1 - pc.t0;
+      rem = L - ((pc.t0 - pc.seg0) * Cfg::kTile + warp * 16);
+    }
+    float m = -INFINITY, l = 0.f;
+    float o[NJ][2];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) o[j][0] = o[j][1] = 0.f;
+    for (int k = 0; k < ntl; ++k, ++T, rem -= Cfg::kTile) {
+      const int s = T % Cfg::kStages;
+      // after a failed wait (the abort flag is set) every later wait fails at once; the warps
+      // still meet at each named barrier below, so the CTA runs to its end
+      if (!mbar_wait(&full_bar[s], static_cast<uint32_t>(T / Cfg::kStages) & 1u, abort_p, kDecodeWaitTimeoutNs))
+        break;
+      {
+        const uint8_t* kt = sK + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
+        const uint8_t* vt = sV + s * Cfg::kTileBytes + warp * 16 * Cfg::kRowBytes;
+        mma_decode_block<D, EB, Cfg::kRowBytes>(kt, vt, rem, qa, cmul, gq, c, m, l, o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+    // l: the 4 threads of a group hold disjoint keys' sums
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+    l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+
+    // the piece again (cheaper than keeping it in registers through the tile loop)
+    const DecodePiece pc = balanced_piece(p, pre, t, hi);
+    t = pc.t1;
+    const int kvh = pc.y / p.n_hblk;
+    const int h0 = kvh * p.g + (pc.y % p.n_hblk) * p.hblk;
+    const int nh = min(p.hblk, (kvh + 1) * p.g - h0);
+    // merge the consumer warps (the area is free: every warp read the previous piece's rows
+    // before it reached this barrier)
+    named_bar_sync(1, 32 * Cfg::kConsumerWarps);
+    if (gq < nh) {
+      float* r = red + (warp * kDecodeMaxHeadsPerCta + gq) * kRed;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        r[VE * (2 * c) + j] = o[j][0];
+        r[VE * (2 * c + 1) + j] = o[j][1];
+      }
+      if (c == 0) {
+        r[D] = m;
+        r[D + 1] = l;
+      }
+    }
+    named_bar_sync(1, 32 * Cfg::kConsumerWarps);
+    const bool to_end = pc.t1 == pc.seg0 + pc.n;
+    const bool whole = pc.t0 == pc.seg0 && to_end;
+    // slot 2c: the piece ends inside its segment; 2c + 1: it starts inside and runs to the end
+    const int slot = 2 * static_cast<int>(blockIdx.x) + (to_end ? 1 : 0);
+    const float vmul = p.v_scale != nullptr ? p.v_scale[static_cast<size_t>(pc.b) * p.Hkv + kvh] : 1.f;
+    for (int idx = threadIdx.x; idx < nh * D; idx += 32 * Cfg::kConsumerWarps) {
+      const int gh = idx / D;
+      const int e = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < Cfg::kConsumerWarps; ++w) M = fmaxf(M, red[(w * kDecodeMaxHeadsPerCta + gh) * kRed + D]);
+      const float base = (M == -INFINITY) ? 0.f : M;
+      float acc = 0.f, lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < Cfg::kConsumerWarps; ++w) {
+        const float* r = red + (w * kDecodeMaxHeadsPerCta + gh) * kRed;
+        const float wt = ex2_approx(r[D] - base);
+        acc += wt * r[e];
+        lsum += wt * r[D + 1];
+      }
+      if (whole) {
+        const size_t row = static_cast<size_t>(pc.b) * p.Hq + h0 + gh;
+        p.o[row * D + e] = __float2bfloat16_rn(acc * vmul / lsum);
+        if (e == 0 && p.lse != nullptr) p.lse[row] = (M + log2f(lsum)) * 0.69314718055994530942f;
+      } else {
+        float* dst = p.part + (static_cast<size_t>(slot) * kDecodeMaxHeadsPerCta + gh) * kRed;
+        dst[e] = acc * vmul;
+        if (e == 0) {
+          dst[D] = M;
+          dst[D + 1] = lsum;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// Merge of the segments that the balanced kernel cut: one CTA of D/64 warps per (sequence,
+// query head), as decode_combine_kernel. A segment held by CTAs c_first < c_last has the
+// partials of slots 2c (c_first <= c < c_last) and 2 c_last + 1, merged in CTA order; a
+// segment inside one CTA was finished there; a sequence without keys gets O = 0 and
+// LSE = -inf. Every CTA between c_first and c_last holds a piece of the segment (no range
+// between them is empty, see BalancedPartition). Launched as a programmatic dependent of the
+// balanced kernel.
+template <int D>
+__global__ void __launch_bounds__(D / 2) decode_balanced_merge_kernel(const BalancedParams p) {
+  constexpr int kGroup = 32;
+  constexpr int kRed = D + 2;
+  __shared__ long long s_sum[2][D / 64];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq;
+  const int h = bh % p.Hq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // tiles before sequence b and in all: the same prefix the balanced kernel formed
+  long long before = 0, total = 0;
+  constexpr int kTile = DecodeCfg<D>::kTile;
+  for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+    const int n = (seq_len_clamped(p.seqlens, bb, p.Lcap) + kTile - 1) / kTile;
+    total += n;
+    if (bb < b) before += n;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
+    total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
+  }
+  if (lane == 0) {
+    s_sum[0][warp] = before;
+    s_sum[1][warp] = total;
+  }
+  __syncthreads();
+  before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < D / 64; ++w) {
+    before += s_sum[0][w];
+    total += s_sum[1][w];
+  }
+  const int e0 = warp * 64 + 2 * lane;
+  __nv_bfloat16* orow = p.o + static_cast<size_t>(bh) * D + e0;
+  const int n = (seq_len_clamped(p.seqlens, b, p.Lcap) + kTile - 1) / kTile;
+  if (n == 0) {  // no key: O = 0, LSE = -inf
+    *reinterpret_cast<uint32_t*>(orow) = 0u;
+    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bh] = -INFINITY;
+    return;
+  }
+  const int kvh = h / p.g;
+  const int within = h % p.g;
+  const int y = kvh * p.n_hblk + within / p.hblk;
+  const int gh = within % p.hblk;
+  const BalancedPartition part(static_cast<int>(p.Y * total), p.G);  // NT >= n >= 1
+  const int seg0 = static_cast<int>(p.Y * before) + y * n;
+  const int c_first = part.cta_of(seg0);
+  const int c_last = part.cta_of(seg0 + n - 1);
+  if (c_first == c_last) return;  // finished by its CTA
+  const int np = c_last - c_first + 1;
+  auto slot_of = [&](int k) { return (k < np - 1) ? 2 * (c_first + k) : 2 * c_last + 1; };
+  float M = -INFINITY, lsum = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
+  for (int g0 = 0; g0 < np; g0 += kGroup) {
+    const int cnt = min(kGroup, np - g0);
+    float2 mlv = make_float2(-INFINITY, 0.f);
+    if (lane < cnt) {
+      const float* r = p.part + (static_cast<size_t>(slot_of(g0 + lane)) * kDecodeMaxHeadsPerCta + gh) * kRed;
+      mlv = make_float2(r[D], r[D + 1]);
+    }
+    float2 v[kGroup];
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) {
+      v[t] = make_float2(0.f, 0.f);
+      if (t < cnt)
+        v[t] = *reinterpret_cast<const float2*>(
+            p.part + (static_cast<size_t>(slot_of(g0 + t)) * kDecodeMaxHeadsPerCta + gh) * kRed + e0);
+    }
+    float mg = mlv.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
+    const float M_new = fmaxf(M, mg);
+    const float w = lane < cnt ? ex2_approx(mlv.x - M_new) : 0.f;
+    float lp = w * mlv.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lp += __shfl_xor_sync(0xFFFFFFFFu, lp, off);
+    const float r = ex2_approx(M - M_new);  // 0 on the first group (M = -inf)
+    float2 a = make_float2(acc.x * r, acc.y * r);
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) {
+      const float wt = __shfl_sync(0xFFFFFFFFu, w, t);
+      if (t < cnt) {
+        a.x = fmaf(wt, v[t].x, a.x);
+        a.y = fmaf(wt, v[t].y, a.y);
+      }
+    }
+    acc = a;
+    lsum = fmaf(lsum, r, lp);
+    M = M_new;
+  }
+  *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc.x / lsum, acc.y / lsum);
+  if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bh] = (M + log2f(lsum)) * 0.69314718055994530942f;
 }
 
 // One CTA of D/64 warps per (sequence, query head); warp w owns output elements [64 w, 64 w + 64),
@@ -866,6 +1282,94 @@ static cudaError_t launch_split_mma(const DecodeParams& p, int B, cudaStream_t s
   return cudaGetLastError();
 }
 
+// Streaming multiprocessors of the current device (queried once per device).
+static int decode_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) {
+    int n = 0;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : 0;
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Workspace of the balanced schedule on the current device: two partial slots per CTA, each
+// kDecodeMaxHeadsPerCta rows of d + 2 floats.
+size_t decode_balanced_workspace_bytes(int d) {
+  const int sms = decode_sm_count();
+  if (sms <= 0) return 0;
+  return static_cast<size_t>(2) * kMmaCtasPerSm * sms * kDecodeMaxHeadsPerCta * (static_cast<size_t>(d) + 2) *
+         sizeof(float);
+}
+int decode_balanced_max_batch() { return kBalancedMaxB; }
+
+template <int D, int EB>
+static cudaError_t launch_balanced(const BalancedParams& p, cudaStream_t stream, int* launched) {
+  using Cfg = DecodeCfg<D, EB, mma_stages<D, EB>()>;
+  const int smem = 2 * Cfg::kStages * Cfg::kTileBytes + 1024 +
+                   Cfg::kConsumerWarps * kDecodeMaxHeadsPerCta * (D + 2) * static_cast<int>(sizeof(float));
+  auto kern = decode_balanced_kernel<D, EB>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<p.G, Cfg::kThreads, smem, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  *launched = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B) * static_cast<unsigned>(p.Hq));
+  cfg.blockDim = dim3(static_cast<unsigned>(D / 2));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, decode_balanced_merge_kernel<D>, p);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  if (err == cudaSuccess) *launched = 2;
+  return err;
+}
+
+// The balanced schedule (num_splits = 0): a persistent grid of kMmaCtasPerSm CTAs per SM.
+static cudaError_t launch_decode_balanced(const void* q, const void* kc, const void* vc, const float* k_scale,
+                                          const float* v_scale, const int* seqlens, void* o, float* lse, int B,
+                                          int Hq, int Hkv, int d, int Lcap, float scale, void* workspace,
+                                          cudaStream_t stream, int* launched) {
+  const int sms = decode_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  if (B > kBalancedMaxB) return cudaErrorInvalidValue;
+  BalancedParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kc = static_cast<const uint8_t*>(kc);
+  p.vc = static_cast<const uint8_t*>(vc);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.seqlens = seqlens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.part = static_cast<float*>(workspace);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = Hq / Hkv;
+  p.n_hblk = (p.g + kDecodeMaxHeadsPerCta - 1) / kDecodeMaxHeadsPerCta;
+  p.hblk = (p.g + p.n_hblk - 1) / p.n_hblk;
+  p.Lcap = Lcap;
+  p.Y = Hkv * p.n_hblk;
+  p.G = kMmaCtasPerSm * sms;
+  p.c = scale * 1.4426950408889634f;
+  const bool fp8 = k_scale != nullptr;
+  if (fp8) return (d == 64) ? launch_balanced<64, 1>(p, stream, launched) : launch_balanced<128, 1>(p, stream, launched);
+  return (d == 64) ? launch_balanced<64, 2>(p, stream, launched) : launch_balanced<128, 2>(p, stream, launched);
+}
+
 // The split kernel's consumers: tensor-core MMAs (decode_split_mma_kernel), unless the
 // environment variable GB300_ATTN_DECODE is "ffma" (decode_split_kernel; the same result up to
 // rounding).
@@ -880,6 +1384,9 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const f
                           const int* seqlens, void* o, float* lse, int B, int Hq, int Hkv, int d, int Lcap,
                           float scale, int S, int C, void* workspace, cudaStream_t stream, int* launched) {
   *launched = 0;
+  if (S == 0)
+    return launch_decode_balanced(q, kc, vc, k_scale, v_scale, seqlens, o, lse, B, Hq, Hkv, d, Lcap, scale, workspace,
+                                  stream, launched);
   const bool fp8 = k_scale != nullptr;
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);

@@ -115,14 +115,17 @@ attn_status attn_fwd_ws(const void* q, const void* k, const void* v, void* o, fl
 /*
  * attn_decode_workspace_size - bytes of scratch attn_decode needs.
  * Returns 0 for invalid arguments. The workspace holds one fp32 partial
- * (m, l, o[d]) per (sequence, query head, split).
+ * (m, l, o[d]) per (sequence, query head, split); for num_splits = 0 (the
+ * balanced schedule) two partials of up to 4 query heads per thread block of
+ * the current device (2 per SM), whatever B and Hq are.
  */
 size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
 
 /*
  * attn_decode_default_splits - a split count that fills the GPU for the given
  * shape (enough thread blocks for every SM several times over). Any value in
- * [1, Lcap/16] is valid; results differ between split counts by rounding only.
+ * [1, Lcap/16] is valid, and so is 0 (the balanced schedule, see attn_decode);
+ * results differ between split counts by rounding only.
  */
 int attn_decode_default_splits(int B, int Hkv, int Lcap);
 
@@ -176,14 +179,26 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
  *   o        bf16 [B, Hq, d]    output (written)
  *   lse      fp32 [B, Hq] or NULL
  *   d 64 or 128, Hq % Hkv == 0, Hq / Hkv <= 8, scale > 0 and finite
- *   num_splits   1 .. ceil(Lcap / 16). Split s covers keys
- *                [s*C, (s+1)*C) with C = ceil(Lcap / num_splits) rounded up
- *                to a multiple of 16; splits are merged in a fixed order, so
- *                the result is deterministic for a given num_splits.
+ *   num_splits   1 .. ceil(Lcap / 16): split s covers keys [s*C, (s+1)*C)
+ *                with C = ceil(Lcap / num_splits) rounded up to a multiple of
+ *                16, one thread block per (split, head block, sequence);
+ *                splits are merged in a fixed order, so the result is
+ *                deterministic for a given num_splits.
+ *                0: the balanced schedule. One persistent thread block per
+ *                resident slot (2 per SM) takes an equal share of the 64-key
+ *                tiles of all (sequence, K/V head block) pairs, cut at tile
+ *                boundaries; a pair that one block holds whole is finished
+ *                there, a pair that share boundaries cut is merged from one
+ *                partial per block in block order (the same rule), so the
+ *                result is deterministic for a given device. For batches of
+ *                very different lengths it avoids the last thread blocks of
+ *                the split schedule running alone. Needs B <= 1024 and fewer
+ *                than 2^31 tiles over all pairs (else ATTN_ERR_UNSUPPORTED).
  *   workspace    device scratch of at least
  *                attn_decode_workspace_size(B, Hq, d, num_splits) bytes, 16-byte
  *                aligned, owned by the caller; it must not be used by another
- *                call that can run at the same time.
+ *                call that can run at the same time. For num_splits = 0 its
+ *                size depends only on d and the current device's SM count.
  */
 attn_status attn_decode(const void* q, const void* kcache, const void* vcache,
                         const int* seqlens, void* o, float* lse,

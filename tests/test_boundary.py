@@ -42,7 +42,11 @@ def test_status_strings(lib):
 def test_workspace_size_formula(lib):
     assert lib.attn_decode_workspace_size(16, 32, 128, 64) == 16 * 32 * 64 * 130 * 4
     assert lib.attn_decode_workspace_size(0, 32, 128, 64) == 0
-    assert lib.attn_decode_workspace_size(1, 1, 64, 0) == 0
+    assert lib.attn_decode_workspace_size(1, 1, 64, -1) == 0
+    # num_splits = 0 is the balanced schedule: two partial slots of 4 heads x (d + 2) floats per
+    # CTA, two CTAs per SM of the current device (0 here, with no device; never below 0)
+    assert lib.attn_decode_workspace_size(1, 1, 64, 0) % (2 * 2 * 4 * 66 * 4) == 0
+    assert lib.attn_decode_workspace_size(1, 1, 96, 0) == 0
 
 
 def test_default_splits_in_range(lib):
@@ -83,7 +87,8 @@ def _dec(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(q=None), 1), (dict(sl=None), 1), (dict(Hq=6, Hkv=4), 1), (dict(S=0), 1),
+    (dict(q=None), 1), (dict(sl=None), 1), (dict(Hq=6, Hkv=4), 1), (dict(S=-1), 1),
+    (dict(S=0, B=1025), 2), (dict(S=0, B=1024, Hkv=8, Hq=16, Lcap=1 << 28), 2),
     (dict(S=17), 1), (dict(Lcap=0), 1), (dict(scale=-1.0), 1), (dict(d=80), 2),
     (dict(Hq=18, Hkv=2), 2), (dict(kc=FAKE + 4), 3), (dict(sl=FAKE + 2), 3),
     (dict(ws=None), 4), (dict(wsb=16), 4), (dict(ws=FAKE + 8), 3),
