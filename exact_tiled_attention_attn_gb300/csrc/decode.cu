@@ -808,6 +808,7 @@ struct BalancedParams {
   __nv_bfloat16* o;  // [B, Hq, D]
   float* lse;        // [B, Hq] or nullptr
   float* part;       // [2 G slots][kDecodeMaxHeadsPerCta heads][D + 2]: o, then m and l
+  int* tile_pre;     // [kBalancedMaxB + 1]: the tile prefix sums of the lengths, for the merge
   int B, Hq, Hkv, g, n_hblk, hblk, Lcap;
   int Y;             // segments per sequence: Hkv * n_hblk (head blocks)
   int G;             // CTAs of the balanced kernel
@@ -927,6 +928,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, EB, mma_stages<D, EB>()>::kThread
   // the previous kernel's writes (the cache, q, the lengths) are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
   balanced_prefix<Cfg::kTile>(p, pre);  // ends with __syncthreads
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b <= p.B; b += blockDim.x) p.tile_pre[b] = pre[b];
   volatile int* abort_p = &abort_flag;
   int lo, hi;
   BalancedPartition(p.Y * pre[p.B], p.G).range(static_cast<int>(blockIdx.x), lo, hi);
@@ -1084,40 +1087,17 @@ template <int D>
 __global__ void __launch_bounds__(D / 2) decode_balanced_merge_kernel(const BalancedParams p) {
   constexpr int kGroup = 32;
   constexpr int kRed = D + 2;
-  __shared__ long long s_sum[2][D / 64];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / p.Hq;
   const int h = bh % p.Hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // tiles before sequence b and in all: the same prefix the balanced kernel formed
-  long long before = 0, total = 0;
-  constexpr int kTile = DecodeCfg<D>::kTile;
-  for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
-    const int n = (seq_len_clamped(p.seqlens, bb, p.Lcap) + kTile - 1) / kTile;
-    total += n;
-    if (bb < b) before += n;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
-    total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
-  }
-  if (lane == 0) {
-    s_sum[0][warp] = before;
-    s_sum[1][warp] = total;
-  }
-  __syncthreads();
-  before = 0;
-  total = 0;
-#pragma unroll
-  for (int w = 0; w < D / 64; ++w) {
-    before += s_sum[0][w];
-    total += s_sum[1][w];
-  }
+  // the balanced kernel's tile prefix sums (its CTA 0 stored them)
+  const int before = p.tile_pre[b];
+  const int total = p.tile_pre[p.B];
   const int e0 = warp * 64 + 2 * lane;
   __nv_bfloat16* orow = p.o + static_cast<size_t>(bh) * D + e0;
-  const int n = (seq_len_clamped(p.seqlens, b, p.Lcap) + kTile - 1) / kTile;
+  const int n = p.tile_pre[b + 1] - before;
   if (n == 0) {  // no key: O = 0, LSE = -inf
     *reinterpret_cast<uint32_t*>(orow) = 0u;
     if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bh] = -INFINITY;
@@ -1127,8 +1107,8 @@ __global__ void __launch_bounds__(D / 2) decode_balanced_merge_kernel(const Bala
   const int within = h % p.g;
   const int y = kvh * p.n_hblk + within / p.hblk;
   const int gh = within % p.hblk;
-  const BalancedPartition part(static_cast<int>(p.Y * total), p.G);  // NT >= n >= 1
-  const int seg0 = static_cast<int>(p.Y * before) + y * n;
+  const BalancedPartition part(p.Y * total, p.G);  // NT >= n >= 1
+  const int seg0 = p.Y * before + y * n;
   const int c_first = part.cta_of(seg0);
   const int c_last = part.cta_of(seg0 + n - 1);
   if (c_first == c_last) return;  // finished by its CTA
@@ -1300,12 +1280,15 @@ static int decode_sm_count() {
 }
 
 // Workspace of the balanced schedule on the current device: two partial slots per CTA, each
-// kDecodeMaxHeadsPerCta rows of d + 2 floats.
+// kDecodeMaxHeadsPerCta rows of d + 2 floats, then the tile prefix sums (kBalancedMaxB + 1 ints).
+static size_t balanced_slot_bytes(int sms, int d) {
+  return static_cast<size_t>(2) * kMmaCtasPerSm * sms * kDecodeMaxHeadsPerCta * (static_cast<size_t>(d) + 2) *
+         sizeof(float);
+}
 size_t decode_balanced_workspace_bytes(int d) {
   const int sms = decode_sm_count();
   if (sms <= 0) return 0;
-  return static_cast<size_t>(2) * kMmaCtasPerSm * sms * kDecodeMaxHeadsPerCta * (static_cast<size_t>(d) + 2) *
-         sizeof(float);
+  return balanced_slot_bytes(sms, d) + (kBalancedMaxB + 4) * sizeof(int);
 }
 int decode_balanced_max_batch() { return kBalancedMaxB; }
 
@@ -1355,6 +1338,7 @@ static cudaError_t launch_decode_balanced(const void* q, const void* kc, const v
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.part = static_cast<float*>(workspace);
+  p.tile_pre = reinterpret_cast<int*>(static_cast<char*>(workspace) + balanced_slot_bytes(sms, d));
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -41,7 +41,8 @@ def main(argv=None):
                                            "kv_quant"], required=True)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--iters", type=int, default=3)
-    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=None,
+                    help="decode: split count; 0 = the balanced schedule (default: the library default count)")
     ap.add_argument("--rows", type=int, default=0, help="rmsnorm: rows T of X[T, 1024] (default: the workload's)")
     args = ap.parse_args(argv)
 
@@ -78,7 +79,7 @@ def main(argv=None):
         shp = W.DECODE_LLAMA
         q, kc, vc, sl = W.decode_inputs(shp)
         q, kc, vc, sld = q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev)
-        S = args.splits or attn.default_splits(shp.B, shp.Hkv, shp.Lcap)
+        S = args.splits if args.splits is not None else attn.default_splits(shp.B, shp.Hkv, shp.Lcap)
         ws = torch.empty(attn.decode_workspace_size(shp.B, shp.Hq, shp.d, S), dtype=torch.uint8, device=dev)
         o = torch.empty_like(q)
         lse = torch.empty(shp.B, shp.Hq, dtype=torch.float32, device=dev)
