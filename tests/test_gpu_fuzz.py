@@ -7,7 +7,9 @@ from a fixed seed, so that the combinations nobody picked get covered too:
 * Tq != Tk on both sides of each other, including lengths below, at and past a tile;
 * causal and not, d = 64 and 128;
 * decode lengths anywhere in [1, Lcap] and split counts up to Lcap / 16, for the bf16 and the
-  E4M3 cache;
+  E4M3 cache, and the balanced schedule (num_splits = 0) over lengths from 0 to Lcap;
+* non-causal prefill with the persistent CTA count capped at random, so that the last round's
+  units are split along the keys and merged;
 * RMSNorm rows and widths on both sides of the block-per-row threshold, with and without the
   residual add.
 
@@ -129,6 +131,73 @@ def test_decode_fp8_random_shapes(attn, case):
     ovc, ovs = oracle.quantize_kv(f64(vc))
     O, L = oracle.decode_fp8(f64(q), okc, ovc, oks, ovs, sl.numpy(), shp.scale)
     assert_attn_close(o, lse, O, L, f"fp8 decode {case[:7]}")
+
+
+def _balanced_cases(n, seed):
+    rnd = random.Random(seed)
+    for _ in range(n):
+        Hkv = rnd.choice([1, 2, 4, 8])
+        g = rnd.choice([1, 2, 3, 4, 6, 8])
+        B = rnd.randint(1, 12)
+        Lcap = rnd.choice([rnd.randint(1, 200), rnd.randint(16, 5000)])
+        lens = [rnd.choice([0, 1, rnd.randint(1, Lcap), Lcap]) for _ in range(B)]
+        yield B, Hkv * g, Hkv, rnd.choice([64, 128]), Lcap, tuple(lens), rnd.random() < 0.5, rnd.randint(0, 10**6)
+
+
+@pytest.mark.parametrize("case", list(_balanced_cases(40, 24601)),
+                         ids=lambda c: "B{}_Hq{}_Hkv{}_d{}_L{}_fp8{}".format(c[0], c[1], c[2], c[3], c[4], int(c[6])))
+def test_decode_balanced_random_shapes(attn, case):
+    B, Hq, Hkv, d, Lcap, lens, fp8, seed = case
+    shp = W.DecodeShape("fuzz", B, Hq, Hkv, d, 1, Lcap, seed)
+    q, kc, vc, sl = W.decode_inputs(shp, seqlens=[max(1, x) for x in lens])
+    sl = torch.tensor(lens, dtype=torch.int32)  # zero lengths too: O = 0, LSE = -inf
+    if fp8:
+        kcodes, ksc = attn.kv_quantize_fp8(kc.to(DEV))
+        vcodes, vsc = attn.kv_quantize_fp8(vc.to(DEV))
+        o, lse = attn.decode_fp8(q.to(DEV), kcodes, vcodes, ksc, vsc, sl.to(DEV), num_splits=0)
+    else:
+        o, lse = attn.decode(q.to(DEV), kc.to(DEV), vc.to(DEV), sl.to(DEV), num_splits=0)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    o, lse = f64(o), f64(lse)
+    zero = [b for b in range(B) if lens[b] == 0]
+    for b in zero:
+        assert np.all(o[b] == 0.0) and np.all(np.isneginf(lse[b])), f"empty sequence {b}"
+    keep = [b for b in range(B) if lens[b] > 0]
+    if not keep:
+        return
+    if fp8:
+        okc, oks = oracle.quantize_kv(f64(kc))
+        ovc, ovs = oracle.quantize_kv(f64(vc))
+        O, L = oracle.decode_fp8(f64(q)[keep], okc[keep], ovc[keep], oks[keep], ovs[keep], sl.numpy()[keep], shp.scale)
+    else:
+        O, L = oracle.decode(f64(q)[keep], f64(kc)[keep], f64(vc)[keep], sl.numpy()[keep], shp.scale)
+    assert_attn_close(o[keep], lse[keep], O, L, f"balanced decode {case[:7]}")
+
+
+def _split_prefill_cases(n, seed):
+    rnd = random.Random(seed)
+    for _ in range(n):
+        Hkv = rnd.choice([1, 2, 3])
+        g = rnd.choice([1, 2, 3, 4])
+        B = rnd.choice([1, 2, 3])
+        Tq = rnd.randint(1, 1200)
+        Tk = rnd.choice([Tq, rnd.randint(1, 2500)])
+        yield B, Hkv * g, Hkv, Tq, Tk, rnd.choice([64, 128]), rnd.randint(1, 24), rnd.randint(0, 10**6)
+
+
+@pytest.mark.parametrize("case", list(_split_prefill_cases(32, 51200)),
+                         ids=lambda c: "B{}_Hq{}_Hkv{}_Tq{}_Tk{}_d{}_ctas{}".format(*c[:7]))
+def test_prefill_split_tail_random_shapes(attn, monkeypatch, case):
+    B, Hq, Hkv, Tq, Tk, d, ctas, seed = case
+    monkeypatch.setenv("GB300_ATTN_PREFILL_CTAS", str(ctas))
+    q, k, v = W.attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=False, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    O, L = oracle.attention(f64(q), f64(k), f64(v), False, scale)
+    assert_attn_close(o, lse, O, L, f"split-tail prefill {case[:7]}")
 
 
 def _norm_cases(n, seed):
