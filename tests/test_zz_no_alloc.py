@@ -8,7 +8,8 @@ middle of a step. attn_decode_noalloc keeps the split partials in a fixed
 
 * on two calls in a row that share the array, the result equals what
   attn_decode returns, and both equal the float64 oracle, at the tolerances of
-  every other GPU test (max |dO| <= 2e-2, mean |dO| <= 2e-3, max |dLSE| <= 1e-3);
+  every other GPU test (max |dO| <= 2e-2, mean |dO| <= 2e-3, max |dLSE| <= 1e-3),
+  for split counts and for the balanced schedule (num_splits = 0);
 * a warmed-up call changes the device's free memory by zero bytes;
 * requests whose partials would not fit are refused before anything runs, and
   the binding's default split count is lowered until they fit.
@@ -118,6 +119,18 @@ def test_matches_attn_decode_and_oracle_on_two_calls_in_a_row(lib):
     # first call's partials, which must not leak into this result
     small = W.DecodeShape("t", 3, 8, 2, 64, 1, 300, 2025)
     _run_pair(lib, torch, small, [1, 150, 300], 7, seed=2025)
+
+
+@pytest.mark.gpu
+def test_balanced_schedule_matches_attn_decode_and_oracle(lib):
+    # num_splits = 0: the balanced schedule's partials and prefix sums also go to the array
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test needs a CUDA device")
+    shape = W.DecodeShape("t", 16, 32, 8, 128, 1024, 4096, 2026)
+    _run_pair(lib, torch, shape, W.decode_lengths(shape), 0, seed=2026)
+    small = W.DecodeShape("t", 5, 8, 2, 64, 1, 300, 2027)
+    _run_pair(lib, torch, small, [1, 150, 300, 64, 65], 0, seed=2027)
 
 
 @pytest.mark.gpu
