@@ -154,11 +154,15 @@ def test_workspace_arguments_are_checked(attn):
     torch.cuda.synchronize()
 
 
-def test_full_size_mha_tail_rows(attn):
-    """Non-causal MHA B8 H12 T4096 d64 on every SM: the last round's units are split; their
-    rows (all row tiles of the last head) against the oracle, and the rest bitwise equal to
-    the unsplit kernel."""
-    shp = W.MHA_GPT2
+@pytest.mark.parametrize("shape", [W.MHA_GPT2, W.AttnShape("non-causal MHA B1 H20 T4096 d128", 1, 20, 20, 4096, 128,
+                                                           False, 3100)],
+                         ids=["mha-b8-h12-d64", "mha-b1-h20-d128"])
+def test_full_size_mha_tail_rows(attn, shape):
+    """Non-causal MHA on every SM (B8 H12 T4096 d64: 1536 units, 16 in the last round; B1 H20
+    T4096 d128: 320 units, 16 in the last round): the last round's units are split; their rows
+    (all row tiles of the last head) against the oracle, and the rest bitwise equal to the
+    unsplit kernel."""
+    shp = shape
     q, k, v = W.attention_inputs(shp)[:3]
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     n0 = attn.kernel_launches()
@@ -184,7 +188,8 @@ def test_full_size_mha_tail_rows(attn):
     O_all, L_all, o_all, l_all = [], [], [], []
     for b, h in heads[:: max(1, len(heads) // 6)] + [heads[-1]]:
         rows = np.nonzero(m[b, h])[0]
-        rows = np.unique(np.concatenate([rows[:2], rows[-2:], rng.choice(rows, 6)]))
+        edges = [r for r in (127, 128, 255, 256, 2047, 2048) if m[b, h, r]]  # tile and piece boundaries
+        rows = np.unique(np.concatenate([rows[:2], rows[-2:], rng.choice(rows, 6), edges]).astype(np.int64))
         Or, Lr = oracle.attention_rows(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, h:h + 1]), f64(v[b:b + 1, h:h + 1]),
                                        0, 0, rows, False, shp.scale)
         O_all.append(Or)
