@@ -46,8 +46,8 @@ WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 # ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md, with
 # the SHA-256 of the kernel's sources (prefill.cu and common.cuh) it was taken with: the figure is
 # reported only while those sources are unchanged.
-PREFILL_TRAFFIC = {"bytes": 284227840 + 82520832,
-                   "sources_sha256": "7b02a129244de3914155143d1d9b3b418560b8c7c1a2cf8423fa9a14154f5b36"}
+PREFILL_TRAFFIC = {"bytes": 282796544 + 82557696,
+                   "sources_sha256": "b10e1f6e995ae4a8b202448b299fed9907eb16b14fefe392e0af1b2104adaa4c"}
 PREFILL_SOURCES = ("prefill.cu", "common.cuh")
 
 

@@ -38,6 +38,12 @@
 // filled runs that round's units as pieces over consecutive key blocks instead, and
 // attn_fwd_merge_kernel combines each unit's pieces (the online-softmax merge).
 //
+// Work distribution: one persistent CTA per SM walks the units in rounds (snake order; causal
+// units heaviest first, non-causal ones (batch, head)-major). A non-causal launch whose last
+// round would be only partly filled runs that round's units as pieces over consecutive key
+// blocks instead, and attn_fwd_merge_kernel combines each unit's pieces (the online-softmax
+// merge).
+//
 // The maximum used as the exponent base is only moved when the new block maximum
 // exceeds it by more than 2^8 (in base 2); the normalised result does not depend on
 // which finite base is subtracted ("Module 07", section "Online softmax: derivation":
@@ -241,9 +247,10 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = tmem_base_holder;
   volatile int* abort_p = &abort_flag;
 
-  // Every role walks the same units in the same order and keeps the barrier phases running
-  // across them: G = index of the unit's key block 0 in this CTA's sequence of key blocks
-  // (a unit with n = max(nkv) has blocks 0..n, so G grows by n + 1 per unit).
+  // Every role walks the same work items (whole units, or pieces of the split units) in the
+  // same order and keeps the barrier phases running across them: G = index of the item's key
+  // block 0 in this CTA's sequence of key blocks (an item with n = max(nkv) has blocks 0..n,
+  // so G grows by n + 1 per item).
   if (warp == kWarpProducer) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
