@@ -650,7 +650,7 @@ def run_gpu(args):
     if not args.no_e2e:
         sshp = W.DecodeShape("short", DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.d, 1024, 2048, DECODE.seed)
         sq, skc, svc, ssl = [t.to(dev) for t in W.decode_inputs(sshp)]
-        sS = attn.default_splits(sshp.B, sshp.Hkv, sshp.Lcap)
+        sS = splits  # the balanced schedule by default (graph replay: 23.3 us per step against 24.7 with 2 splits)
         sws = torch.empty(attn.decode_workspace_size(sshp.B, sshp.Hq, sshp.d, sS), dtype=torch.uint8, device=dev)
         so, sl_ = torch.empty_like(sq), torch.empty(sshp.B, sshp.Hq, dtype=torch.float32, device=dev)
         nstep = 20
@@ -684,6 +684,7 @@ def run_gpu(args):
         graph_ms = a.elapsed_time(b) / nstep
         s_bytes = 4 * sshp.Hkv * sshp.d * int(ssl.sum().item())
         short = {"workload": "flash-decoding B16 Hq32 Hkv8 d128 L~U[1024,2048]", "num_splits": sS,
+                 "kernels": decode_kernels(sS, 2),
                  "eager_us_per_step": round(1e3 * eager_ms, 2), "graph_us_per_step": round(1e3 * graph_ms, 2),
                  "eager_GB/s": round(s_bytes / (eager_ms * 1e-3) / 1e9, 1),
                  "graph_GB/s": round(s_bytes / (graph_ms * 1e-3) / 1e9, 1),
