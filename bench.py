@@ -46,8 +46,8 @@ WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 # ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md, with
 # the SHA-256 of the kernel's sources (prefill.cu and common.cuh) it was taken with: the figure is
 # reported only while those sources are unchanged.
-PREFILL_TRAFFIC = {"bytes": 282796544 + 82557696,
-                   "sources_sha256": "b10e1f6e995ae4a8b202448b299fed9907eb16b14fefe392e0af1b2104adaa4c"}
+PREFILL_TRAFFIC = {"bytes": 283972352 + 82207744,
+                   "sources_sha256": "d15de67f4d8fc38dcfefed5c231711f99f5e2fb865a8d1f003a5d110d6cf0e41"}
 PREFILL_SOURCES = ("prefill.cu", "common.cuh")
 
 
