@@ -180,6 +180,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// 32-byte global store with an L2 eviction policy (dst 32-byte aligned): a whole sector per
+// thread, half the store instructions of the 16-byte form.
+__device__ __forceinline__ void st_global_v8_hint(void* dst, const uint32_t* w, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(policy)
+               : "memory");
+}
+
 // 16-byte global store with an L2 eviction policy.
 __device__ __forceinline__ void st_global_v4_hint(void* dst, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x), "r"(v.y),
