@@ -5,7 +5,7 @@ The fixed tests pick shapes by hand (tile edges, tails, groupings). Here the sha
 from a fixed seed, so that the combinations nobody picked get covered too:
 * batch and head counts, with the query heads a multiple of the K/V heads;
 * Tq != Tk on both sides of each other, including lengths below, at and past a tile;
-* causal and not, d = 64 and 128;
+* causal and not, d = 64 and 128; the output 32-byte aligned or offset by 16 bytes;
 * decode lengths anywhere in [1, Lcap] and split counts up to Lcap / 16, for the bf16 and the
   E4M3 cache, and the balanced schedule (num_splits = 0) over lengths from 0 to Lcap;
 * non-causal prefill with the persistent CTA count capped at random, so that the last round's
@@ -53,11 +53,15 @@ def test_prefill_random_shapes(attn, case):
     B, Hq, Hkv, Tq, Tk, d, causal, seed = case
     q, k, v = W.attention_inputs_custom(B, Hq, Hkv, Tq, Tk, d, seed)
     scale = 1.0 / math.sqrt(d)
-    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+    # O either 32-byte aligned (32-byte stores) or offset by 16 bytes (16-byte stores)
+    off = 8 if seed % 2 else 0
+    flat = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=DEV)
+    out = flat[off:off + q.numel()].view(q.shape)
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale, out=out)
     torch.cuda.synchronize()
     assert attn.last_device_error() == 0
     O, L = oracle.attention(f64(q), f64(k), f64(v), causal, scale)
-    assert_attn_close(o, lse, O, L, f"prefill {case[:7]}")
+    assert_attn_close(o, lse, O, L, f"prefill {case[:7]} O offset {2 * off} B")
 
 
 def _grad_close(got, want, what):
