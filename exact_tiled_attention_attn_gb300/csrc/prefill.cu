@@ -593,6 +593,17 @@ __global__ void __launch_bounds__(352, 1)
         const float inv_l = 1.f / l_run;
         const bool store = row < p.Tq;
         const size_t orow = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row;
+        // Each thread owns one row, so a plain store of a warp covers 32 rows. When O is 32-byte
+        // aligned, lanes 2i and 2i + 1 (rows 2i, 2i + 1) swap one 32-byte half of each 64-byte
+        // chunk (one shuffle per word) and each 32-byte store then writes 64 contiguous bytes of
+        // one row from the pair. The O stores sit on the softmax warps' path from a unit's last
+        // block to the next unit's first P; measured on causal GQA B2 Hq32 T8192: 16-byte stores
+        // 1625-1650 TFLOP/s, 32-byte stores 1671-1692, with the swap 1692-1697 (B1 Hq16 T4096:
+        // 1185 -> 1228).
+        const bool odd = (lane & 1) != 0;
+        const int row_e = row0 + (row_in_tile & ~1);  // the pair's even row
+        const bool st_e = row_e < p.Tq, st_o = row_e + 1 < p.Tq;
+        const size_t orow_e = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row_e;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
@@ -601,22 +612,24 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             pk[k] = pack_bf16x2(__uint_as_float(ov[2 * k]) * inv_l, __uint_as_float(ov[2 * k + 1]) * inv_l);
-          if (store) {
-            // each thread writes its own row, so a warp's store covers 32 rows: 32-byte stores
-            // (whole sectors, half the instructions) when O allows them. Measured on causal GQA
-            // B2 Hq32 T8192: 1625-1650 -> 1671-1692 TFLOP/s; the O stores sit on the softmax
-            // warps' path from a unit's last block to the next unit's first P.
-            if (p.o_v8) {
-              uint32_t* dst = reinterpret_cast<uint32_t*>(p.o + orow * D + cc * 32);
-              st_global_v8_hint(dst, pk, o_policy);
-              st_global_v8_hint(dst + 8, pk + 8, o_policy);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + cc * 32);
+          if (p.o_v8) {
+            // after the swap pk[0..7] is this lane's 32 bytes of the even row, pk[8..15] its 32
+            // bytes of the odd row (the even lane holds both rows' first halves, the odd lane
+            // both second halves)
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                st_global_v4_hint(dst + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]),
-                                  o_policy);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t r = __shfl_xor_sync(0xFFFFFFFFu, odd ? pk[k] : pk[8 + k], 1);
+              if (odd) pk[k] = r; else pk[8 + k] = r;
             }
+            uint32_t* base = reinterpret_cast<uint32_t*>(p.o + orow_e * D + cc * 32) + (odd ? 8 : 0);
+            if (st_e) st_global_v8_hint(base, pk, o_policy);
+            if (st_o) st_global_v8_hint(base + D / 2, pk + 8, o_policy);
+          } else if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D + cc * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              st_global_v4_hint(dst + v, make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]),
+                                o_policy);
           }
         }
         if (store && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
