@@ -99,6 +99,7 @@ struct BwdParams {
   int B, Hq, Hkv, Tq, Tk, g, causal;
   float c;             // scale * log2(e)
   float scale;
+  int out_v8;          // dq, dk and dv are 32-byte aligned: rows are written with 32-byte stores
 };
 
 // Shared-memory descriptors of a tile at byte offset `off` from the descriptor of tile 0: the start
@@ -134,11 +135,30 @@ __device__ __forceinline__ void bwd_mma_accumulate_split(uint32_t d_tmem, uint32
             (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// 32-byte global store (dst 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Half `half` (columns [half*D/2, (half+1)*D/2)) of one row (this thread's TMEM lane) of a
-// [128 x D] fp32 accumulator, times `mul`, to bf16 in global.
+// [128 x D] fp32 accumulator, times `mul`, to bf16 in global. Called by every thread of the
+// warp (the TMEM load and the shuffles are warp-collective); `store` says whether this thread's
+// row exists. With v8 (the outputs 32-byte aligned) the two lanes of each pair (rows r, r + 1,
+// the same half) swap one 32-byte half of each 64-byte chunk, so that each 32-byte store
+// writes 64 contiguous bytes of one row (measured: causal GQA B2 Hq32 T8192 backward
+// 2.347-2.368 -> 2.318-2.326 ms, B1 Hq16 T4096 0.181-0.183 -> 0.178 ms, bitwise equal).
 template <int D>
 __device__ __forceinline__ void bwd_store_row(uint32_t t_acc, float mul, bool have, bool store, __nv_bfloat16* dst,
-                                              int half) {
+                                              int half, bool v8) {
+  const bool odd = (threadIdx.x & 1) != 0;
+  // the pair's two rows: their store flags and addresses
+  const bool store_p = __shfl_xor_sync(0xFFFFFFFFu, store ? 1 : 0, 1) != 0;
+  const unsigned long long dst_p = __shfl_xor_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(dst), 1);
+  __nv_bfloat16* dst_e = odd ? reinterpret_cast<__nv_bfloat16*>(dst_p) : dst;
+  __nv_bfloat16* dst_o = odd ? dst : reinterpret_cast<__nv_bfloat16*>(dst_p);
+  const bool st_e = odd ? store_p : store, st_o = odd ? store : store_p;
 #pragma unroll
   for (int c2 = 0; c2 < D / 64; ++c2) {
     const int cc = half * (D / 64) + c2;
@@ -152,7 +172,16 @@ __device__ __forceinline__ void bwd_store_row(uint32_t t_acc, float mul, bool ha
     uint32_t pk[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
-    if (store) {
+    if (v8) {
+      // after the swap pk[0..7] is this lane's 32 bytes of the even row, pk[8..15] of the odd row
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t r = __shfl_xor_sync(0xFFFFFFFFu, odd ? pk[k] : pk[8 + k], 1);
+        if (odd) pk[k] = r; else pk[8 + k] = r;
+      }
+      if (st_e) st_global_v8(reinterpret_cast<uint32_t*>(dst_e + cc * 32) + (odd ? 8 : 0), pk);
+      if (st_o) st_global_v8(reinterpret_cast<uint32_t*>(dst_o + cc * 32) + (odd ? 8 : 0), pk + 8);
+    } else if (store) {
       uint4* o = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
       for (int w = 0; w < 4; ++w) o[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
@@ -464,9 +493,10 @@ __global__ void __launch_bounds__(352, 1)
     tc_fence_after();
     const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Tk + key;
     const bool have = ok && n_it > 0;
-    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, 1.f, have, key_ok && (ok || n_it == 0), p.dv + orow * D, half);
+    bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc0, 1.f, have, key_ok && (ok || n_it == 0), p.dv + orow * D, half,
+                     p.out_v8 != 0);
     bwd_store_row<D>(tmem + lane_off + Cfg::kTmAcc1, p.scale, have, key_ok && (ok || n_it == 0), p.dk + orow * D,
-                     half);
+                     half, p.out_v8 != 0);
     tc_fence_before();
   }
   __syncthreads();
@@ -718,7 +748,7 @@ __global__ void __launch_bounds__(352, 1)
     if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_done, 0, abort_p, kBwdWaitTimeoutNs));
     tc_fence_after();
     bwd_store_row<D>(tmem + lane_off + Cfg::kTmDq, p.scale, ok && n_j > 0, q_ok && (ok || n_j == 0),
-                     p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D, half);
+                     p.dq + ((static_cast<size_t>(b) * p.Hq + h) * p.Tq + q) * D, half, p.out_v8 != 0);
     tc_fence_before();
   }
   __syncthreads();
@@ -770,6 +800,11 @@ cudaError_t launch_attn_bwd(const void* q, const void* k, const void* v, const v
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  // rows are d * 2 bytes apart (a multiple of 32): every row is 32-byte aligned iff its array is
+  p.out_v8 = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) %
+                  32 == 0)
+                 ? 1
+                 : 0;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -88,3 +88,22 @@ def test_backward_zero_upstream_gradient_and_determinism(attn):
     b = attn.bwd(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_backward_outputs_offset_by_16_bytes(attn, d, causal):
+    # 32-byte-aligned gradients are written with 32-byte stores (lane pairs swapping halves);
+    # one gradient offset by 16 bytes sends all three through 16-byte stores: bitwise the same
+    q, k, v = W.attention_inputs_custom(1, 4, 2, 333, 333, d, 4200 + d)
+    do = W.grad_output(1, 4, 333, d, 4200 + d)
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
+    o, lse = attn.fwd(qd, kd, vd, causal=causal)
+    ref = attn.bwd(qd, kd, vd, o, lse, dod, causal=causal)
+    flat = torch.empty(k.numel() + 8, dtype=torch.bfloat16, device=DEV)
+    dk16 = flat[8:].view(k.shape)
+    assert dk16.data_ptr() % 32 == 16
+    got = attn.bwd(qd, kd, vd, o, lse, dod, causal=causal, dk=dk16)
+    torch.cuda.synchronize()
+    assert attn.last_device_error() == 0
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
