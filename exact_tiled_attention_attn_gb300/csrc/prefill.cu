@@ -9,9 +9,10 @@
 // entirely above the diagonal are never visited when causal; the element mask is
 // applied only on blocks that cross the diagonal or the end of the keys.
 //
-// How it maps onto the GPU (one CTA per work unit of two 128-row query tiles that
-// share one K/V stream: two query heads of the same K/V group at the same rows, or,
-// when the group size is odd, two consecutive row tiles of one head):
+// How it maps onto the GPU (a work unit is two 128-row query tiles that share one K/V
+// stream: two query heads of the same K/V group at the same rows, or, when the group
+// size is odd, two consecutive row tiles of one head; each persistent CTA runs its units
+// one after another):
 //   warp 1      TMA producer: Q tiles once, then K and V tiles into one ring of slots
 //               (128-byte swizzled boxes of 64 columns x 128 rows).
 //   warp 0      MMA issuer (one thread issues): S_q = Q_q K^T into TMEM (fp32), then
@@ -32,7 +33,9 @@
 //               row (TMEM lane), so row max and row sum need no shuffles; P is
 //               written back into the TMEM columns of S and its readiness goes to
 //               warp 0 through a named barrier shared by the tile's four warps and the
-//               issuer; O is rescaled in TMEM.
+//               issuer; O is rescaled in TMEM. At the end of a unit they write O with
+//               32-byte stores, lane pairs swapping halves so that each store covers 64
+//               contiguous bytes of a row.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+d) O1 [256+d,256+2d);
 // P_q aliases the first 64 columns of S_q.
 //
