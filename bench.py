@@ -46,8 +46,8 @@ WORKLOAD = (f"{PREFILL.name} + {DECODE.name} + {NORM.name}")
 # ncu capture summarised in profiles/attn_fwd_kernel_d128_causal_gqa_B2_Hq32_Hkv8_T8192.md, with
 # the SHA-256 of the kernel's sources (prefill.cu and common.cuh) it was taken with: the figure is
 # reported only while those sources are unchanged.
-PREFILL_TRAFFIC = {"bytes": 292718080 + 83002624,
-                   "sources_sha256": "b969a60880872f56b3d1ab2dfdd6c2a1554b4c5e8b564152b007120edb71f580"}
+PREFILL_TRAFFIC = {"bytes": 301086208 + 84741376,
+                   "sources_sha256": "c685f32cca8987fdfe871078fe20a8e78894b86cec5b727e6b6552f30c9a6827"}
 PREFILL_SOURCES = ("prefill.cu", "common.cuh")
 
 

@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(352, 1)
         // O holds the sum up to block j-1 relative to the old base; PV_q(j-1) was issued before
         // S_q(j), so it has completed by now. Rescale in TMEM (after P is written, so the
         // registers of S are free).
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
           tmem_ld32(t_o + cc * 32, ov);
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(352, 1)
         const float inv_l = 1.f / l_run;
         const size_t prow = (static_cast<size_t>(unit_index(round) - p.full_units) * 2 + q) * 128 + row_in_tile;
         float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
-#pragma unroll
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
           tmem_ld32(t_o + cc * 32, ov);
@@ -607,7 +607,9 @@ __global__ void __launch_bounds__(352, 1)
         const int row_e = row0 + (row_in_tile & ~1);  // the pair's even row
         const bool st_e = row_e < p.Tq, st_o = row_e + 1 < p.Tq;
         const size_t orow_e = (static_cast<size_t>(u.b) * p.Hq + head) * p.Tq + row_e;
-#pragma unroll
+        // the epilogue's loops (and the O rescale's) stay rolled: they run once per unit (or
+        // rarely), and unrolled they made the kernel's code larger and the softmax role spill
+#pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
           tmem_ld32(t_o + cc * 32, ov);
