@@ -69,7 +69,8 @@ typedef enum {
  *   scale  > 0 and finite (1/sqrt(d) for standard attention)
  * Arithmetic: bf16 inputs, fp32 scores and running statistics, P rounded to
  * bf16 for the P.V product, fp32 accumulation, O rounded once to bf16.
- * q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
+ * q, k, v, o must be 16-byte aligned; lse 4-byte aligned. An o that is 32-byte aligned
+ * is written with 32-byte stores (faster; the result is the same either way).
  */
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int Tq, int Tk, int d,
@@ -147,6 +148,8 @@ int attn_decode_default_splits(int B, int Hkv, int Lcap);
  *   query i iff j <= i). B*Hq <= 65535.
  *   workspace   device scratch of attn_bwd_workspace_size(B, Hq, Tq) bytes,
  *               16-byte aligned, owned by the caller (holds D_i).
+ * All pointers 16-byte aligned; when dq, dk and dv are all 32-byte aligned the
+ * gradients are written with 32-byte stores (faster; the same result).
  * Arithmetic: P and dS rounded to bf16 for the tensor-core products, fp32
  * accumulation, outputs rounded once to bf16. Three kernel launches; the
  * result does not depend on their timing (no atomics).
